@@ -1,0 +1,228 @@
+/*
+ * moe.h — C ABI of libmoe: the forward pass of a sparse Mixture-of-Experts
+ * FFN layer on one NVIDIA B300 (sm_103a).
+ *
+ * Sources (web pages on Mixture-of-Experts layers; cited by title + section):
+ *   [MoE核心思想]  "MoE 的核心思想" (wmrh.cn/news/98181): 公式表达重点,
+ *                  具体数值示例, 专家容量, 辅助损失公式.
+ *   [稀疏激活原理] "MoE 混合专家模型稀疏激活的架构原理与负载均衡挑战"
+ *                  (mzlw.cn/news/6844): §2.1 Top-K 路由的决策流程,
+ *                  §2.2 负载均衡损失, §2.3 容量因子与 Token 丢弃,
+ *                  §三 MoE 层的生产级 PyTorch 实现 (classes Expert,
+ *                  MoERouter, MoELayer).
+ *   [概念卡]       "混合专家模型（Mixture of Experts, MoE）"
+ *                  (learnagent.wiki): 结构 2 路由器, 结构 3 Top-K 选择与输出融合,
+ *                  运行示例 (minimal MoELayer).
+ *   [替代FFN]      "MoE 如何替代 FFN？它解决了什么问题？带来哪些新挑战？"
+ *                  (mstx.cn/posts/467.html): §1 标准 FFN, §2 MoE 如何替代 FFN.
+ *
+ * Notation: T tokens, d = d_model, N experts, K = top-K, F = d_ff,
+ * C = per-expert capacity, A = number of kept (token, rank) assignments.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Memory: the caller owns every buffer. The library never allocates or
+ *    frees device memory. All tensor pointers are DEVICE pointers, 16-byte
+ *    aligned, row-major and dense (no strides). Scratch space is the caller's
+ *    workspace `ws` of at least moe_workspace_size(cfg) bytes, 256-byte
+ *    aligned; its contents on entry are ignored.
+ *  - Asynchrony: every call only enqueues kernels on `stream` (0 = legacy
+ *    default stream) and returns. Results are valid after the stream is
+ *    synchronised.
+ *  - Errors: every argument error that the host can see (NULL pointer,
+ *    misalignment, bad sizes, unsupported combination) is returned before
+ *    anything is launched. Errors found on the device (a bounded wait that
+ *    timed out, a non-finite router logit, an expert index out of range in
+ *    moe_dispatch's input) are OR-ed as (1u << code) into *stats->status
+ *    when stats and stats->status are non-NULL; read it after a sync.
+ *    The caller zeroes *status before the call if it wants a fresh word.
+ *    No C++ exception crosses this ABI.
+ *  - Limits: 1 <= K <= min(N, 8); N <= 256; 1 <= T <= 2^24 (T = 0 is
+ *    accepted and does nothing); d % 8 == 0 for bf16, d % 4 == 0 for fp32;
+ *    F % 4 == 0.
+ *  - Determinism: every result is bitwise reproducible run to run (fixed
+ *    reduction orders, no floating-point atomics).
+ */
+#ifndef MOE_B300_H_
+#define MOE_B300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream); kept opaque so that this
+ * header does not need the CUDA headers. */
+typedef void* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,     /* bad argument (NULL, alignment, size)          */
+  MOE_ERR_UNSUPPORTED = 2, /* valid, but outside the limits above           */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime call failed (e.g. launch)      */
+  MOE_ERR_TIMEOUT = 4,     /* device: a bounded wait gave up (status word)  */
+  MOE_ERR_NONFINITE = 5,   /* device: a router logit was NaN or infinite    */
+  MOE_ERR_WORKSPACE = 6,   /* workspace NULL, misaligned or too small       */
+  MOE_ERR_INDEX = 7        /* device: an expert index outside [0, N)        */
+} moe_status;
+
+enum { MOE_F32 = 0, MOE_BF16 = 1 };      /* dtype of x, expert weights, y   */
+enum { MOE_SWIGLU = 0, MOE_GELU = 1 };   /* expert activation               */
+
+/* Layer configuration (plain old data). */
+typedef struct {
+  int32_t T;          /* tokens (batch * sequence, flattened)               */
+  int32_t d_model;    /* d                                                  */
+  int32_t d_ff;       /* F, expert hidden width                             */
+  int32_t n_experts;  /* N                                                  */
+  int32_t top_k;      /* K                                                  */
+  int32_t dtype;      /* MOE_F32 | MOE_BF16                                 */
+  int32_t activation; /* MOE_SWIGLU | MOE_GELU                              */
+  int32_t has_bias;   /* expert biases present (GELU experts only)          */
+  float capacity_factor; /* CF; <= 0 or +inf means no capacity limit       */
+  float alpha;        /* coefficient of the load-balance loss               */
+  int32_t add_residual; /* 1: y = x + sum_k g*E(x); a fully dropped token's
+                           output is then x itself                          */
+} moe_config;
+
+/* Device-side statistics; every member is a caller-owned DEVICE pointer and
+ * may be NULL (that output is skipped). The whole struct pointer may be NULL.
+ *   count[N]   assignments routed to each expert before capacity (int32)
+ *   kept[N]    assignments each expert keeps after capacity (int32)
+ *   n_dropped  assignments dropped by capacity (one int32)
+ *   f[N]       count / (T*K)                            (fp32)
+ *   P[N]       mean over tokens of the router softmax   (fp32)
+ *   l_aux      alpha * N * sum_e f[e]*P[e]               (one fp32)
+ *   status     device error bits, (1u << moe_status)     (one uint32)   */
+typedef struct {
+  int32_t* count;
+  int32_t* kept;
+  int32_t* n_dropped;
+  float* f;
+  float* P;
+  float* l_aux;
+  uint32_t* status;
+} moe_stats;
+
+/* Expert weights, stacked over experts, in the nn.Linear (out, in) layout of
+ * each expert ([稀疏激活原理] §三 class Expert; [概念卡] 运行示例).
+ * Element type is cfg->dtype. Unused members are NULL.
+ *   SwiGLU: w_gate [N][F][d], w_up [N][F][d], w_down [N][d][F]
+ *   GELU:   w1 [N][F][d], w2 [N][d][F]; biases b1 [N][F], b2 [N][d]
+ *           (same dtype), required iff cfg->has_bias.                      */
+typedef struct {
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+  const void* w1;
+  const void* b1;
+  const void* w2;
+  const void* b2;
+} moe_expert_weights;
+
+/* Bytes of workspace that moe_forward needs for cfg (an upper bound for the
+ * other entry points too). Pure host function; returns 0 if cfg is invalid.
+ * It covers x_perm [A_max][d], h [A_max][F] and o [A_max][d] fp32, where
+ * A_max = min(T*K, N*C). */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Capacity C per expert: floor(K * CF * T / N), computed exactly on the
+ * rational value of the float CF; INT32_MAX when CF <= 0 or CF = +inf.
+ * [稀疏激活原理] §2.3 (capacity_i formula) and §三 MoELayer.forward
+ * (capacity = int(top_k / num_experts * capacity_factor * num_tokens), with
+ * num_tokens = batch * seq_len). Returns -1 if cfg is invalid. */
+int32_t moe_capacity(const moe_config* cfg);
+
+/* Router: logits = x W_r^T (+ b_r), softmax over the N experts, top-K of the
+ * logits (ties -> lower expert index; ranked by descending logit), gates =
+ * softmax over the K selected logits (the renormalised gate weights), and
+ * the load-balance statistics count, f, P, l_aux.
+ * [稀疏激活原理] §2.1 (logits = x·W_r, Top-K, then softmax) and §2.2
+ * (L_aux = alpha·N·Σ f_i·P_i); [概念卡] 结构 2 (G(x) = Softmax(W_r·x)) and
+ * 运行示例 (softmax -> topk -> renormalise); [MoE核心思想] 公式表达重点 and
+ * 具体数值示例 (8 experts, top-2, gates 0.67 / 0.33).
+ *   x    [T][d]  cfg->dtype        w_r [N][d] fp32      b_r [N] fp32 or NULL
+ *   idx  [T][K]  int32 (out)       gate [T][K] fp32 (out)
+ *   stats: count, f, P, l_aux, status are written (kept/n_dropped are not).
+ * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE,
+ * MOE_ERR_CUDA; device: MOE_ERR_NONFINITE. */
+moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r,
+                     const float* b_r, int32_t* idx, float* gate,
+                     moe_stats* stats, void* ws, moe_stream_t stream);
+
+/* Capacity-limited dispatch. Assignments are visited rank-major (k = 0..K-1,
+ * then t = 0..T-1); an assignment (t, k) to expert e is kept iff fewer than C
+ * earlier assignments went to e. Kept assignments of expert e occupy the
+ * contiguous slots [offsets[e], offsets[e+1]) in that visiting order, and
+ * x_perm[slot] = x[t]. Dropped assignments get slot_of = -1 and contribute
+ * nothing to y (the residual carries the token, [稀疏激活原理] §2.3).
+ * [稀疏激活原理] §2.3 and §三 MoELayer.forward (outer loop over top-k rank,
+ * tokens in ascending order, truncation at capacity).
+ *   x [T][d] cfg->dtype, idx [T][K] int32 (values in [0, N))
+ *   offsets [N+1] int32 (out), slot_of [T][K] int32 (out),
+ *   token_of_slot [A_max] int32 (out, first offsets[N] valid),
+ *   x_perm [A_max][d] cfg->dtype (out).
+ *   stats: count, kept, n_dropped, status are written.
+ * Errors: as moe_route; device: MOE_ERR_INDEX (bad idx value; that
+ * assignment is treated as dropped). */
+moe_status moe_dispatch(const moe_config* cfg, const void* x,
+                        const int32_t* idx, int32_t* offsets, int32_t* slot_of,
+                        int32_t* token_of_slot, void* x_perm, moe_stats* stats,
+                        void* ws, moe_stream_t stream);
+
+/* Grouped expert FFN over the permuted tokens: for every expert e and every
+ * slot s in [offsets[e], offsets[e+1]),
+ *   SwiGLU: o[s] = W_down,e (silu(W_gate,e x) * (W_up,e x))
+ *   GELU:   o[s] = W2,e gelu_erf(W1,e x + b1,e) + b2,e
+ * with x = x_perm[s]; silu(a) = a / (1 + e^-a); gelu_erf(z) =
+ * z/2 (1 + erf(z / sqrt 2)). The hidden activation h is rounded to cfg->dtype
+ * (bf16 or fp32) before the down projection; o is fp32.
+ * [稀疏激活原理] §三 class Expert (SwiGLU); [概念卡] 运行示例
+ * (Linear -> GELU -> Linear); [替代FFN] §1 (FFN(x) = W_2 act(W_1 x)).
+ *   x_perm [A_max][d] cfg->dtype, offsets [N+1] int32 (device, as written by
+ *   moe_dispatch), o [A_max][d] fp32 (out). Rows past offsets[N] untouched.
+ * Errors: as moe_route; device: MOE_ERR_TIMEOUT. */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm,
+                          const int32_t* offsets,
+                          const moe_expert_weights* weights, float* o,
+                          moe_stats* stats, void* ws, moe_stream_t stream);
+
+/* Gate-weighted combine: y[t] = sum over k ascending with slot_of[t][k] >= 0
+ * of gate[t][k] * o[slot_of[t][k]], accumulated in fp32 and rounded once to
+ * cfg->dtype; plus x[t] when cfg->add_residual. No atomics.
+ * [概念卡] 结构 3 (y = Σ_{i∈TopK} G(x)_i E_i(x)); [替代FFN] §2 (MoE(x) formula);
+ * [稀疏激活原理] §2.1.
+ *   o [A_max][d] fp32, slot_of [T][K] int32, gate [T][K] fp32,
+ *   x [T][d] (read only if add_residual; may be NULL otherwise),
+ *   y [T][d] cfg->dtype (out).
+ * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+moe_status moe_combine(const moe_config* cfg, const float* o,
+                       const int32_t* slot_of, const float* gate,
+                       const void* x, void* y, moe_stream_t stream);
+
+/* The whole layer: moe_route -> moe_dispatch -> moe_expert_ffn ->
+ * moe_combine on one stream, with every intermediate in the workspace.
+ * [稀疏激活原理] §三 MoELayer.forward; [概念卡] 核心原理 (four steps).
+ *   x [T][d], w_r [N][d] fp32, b_r [N] fp32 or NULL, weights as above,
+ *   y [T][d] (out), stats (all members optional), ws >= moe_workspace_size.
+ * Errors: the union of the above. */
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r,
+                       const float* b_r, const moe_expert_weights* weights,
+                       void* y, moe_stats* stats, void* ws,
+                       moe_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. Never NULL. */
+const char* moe_status_string(moe_status s);
+
+/* 1 if the expert FFN of cfg runs on the tcgen05 tensor-core path, 0 if it
+ * runs on the CUDA-core path (fp32 configurations, or shapes whose d is not a
+ * multiple of 64 or F not a multiple of 128), -1 if cfg is invalid. */
+int32_t moe_ffn_uses_tensor_cores(const moe_config* cfg);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H_ */
