@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse-MoE forward layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step = one moe_forward over one batch of the workload (router, capacity
+dispatch, grouped expert FFN, combine, statistics) with every input resident
+in HBM. The default workload is the Mixtral-shaped prefill layer (T=4096,
+d=4096, N=8, K=2, SwiGLU F=14336, bf16), seeded synthetic data.
+
+Timing: W untimed warm-up steps; then exactly K steps between a barrier and
+a device synchronise on both sides. Before each step a 256 MB buffer is
+written (L2 is 126 MB) outside the step's CUDA-event interval; the step time
+is the interval between events recorded on the launch stream by the library
+at the step's start and end. value = tokens of all ranks / max over ranks of
+the summed step time. The library's trace events also time each stage; the
+dominant kernel's roofline fraction uses that kernel's own interval.
+
+e2e: the same metric through MoELayer.forward_host: pinned host x copied in,
+the layer, y and L_aux copied out, per step, wall clock with a sync per step.
+
+--impl reference: the float64 CPU oracle, unchanged, timed on this host's
+cores on a bounded token sample of the same workload (rank 0 only).
+
+With torchrun (N > 1) every rank runs its own replica of the layer on its
+own GPU (the layer has no cross-token exchange): weak scaling, no collective
+on the data path; only the timing is reduced across ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import moe_inputs  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec and % of roofline (TFLOP/s or HBM GB/s), 1×B300"
+UNIT = "tokens/s"
+FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ----------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Maximum of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region (read-only NVML queries)
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock"}
+
+    def __init__(self, period_s=0.02):
+        self.period = period_s
+        self.samples = []
+        self.reason_bits = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.error = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nvml = pynvml
+            self.handle = self._handle()
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # no NVML: report nothing rather than guess
+            self.nvml = None
+            self.error = f"nvml unavailable: {e}"
+
+    def _handle(self):
+        p = self.nvml
+        try:
+            uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            return p.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode())
+        except Exception:
+            return p.nvmlDeviceGetHandleByIndex(0)
+
+    def _run(self):
+        p = self.nvml
+        while not self._stop.is_set():
+            try:
+                mhz = p.nvmlDeviceGetClockInfo(self.handle, p.NVML_CLOCK_SM)
+                try:
+                    bits = p.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
+                except Exception:
+                    bits = p.nvmlDeviceGetCurrentClocksThrottleReasons(self.handle)
+                self.samples.append(mhz)
+                self.reason_bits |= int(bits)
+            except Exception as e:
+                self.error = str(e)
+                return
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+
+    def summary(self):
+        reasons = [name for bit, name in self.REASONS.items()
+                   if self.reason_bits & bit and name != "gpu_idle"]
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+        if self.error:
+            out["note"] = self.error
+        return out
+
+
+# ----------------------------------------------------------------------------
+# roofline bookkeeping
+# ----------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained",
+                                                     p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+def algorithmic_work(w, kept, offsets_active):
+    """FLOPs and bytes the layer's definition needs (kept assignments only).
+
+    gate/up GEMM: flops 2*A*d*(2F); bytes: the active experts' gate and up
+    weights once, x_perm read once, h written once (bf16).
+    down GEMM:    flops 2*A*F*d; bytes: active experts' down weights, h read,
+                  o written (fp32).
+    layer:        flops 2*A*d*F*mats; bytes: active experts' weights once, x
+                  read once, y written once, the router weights."""
+    A = int(kept)
+    es = 2 if w.dtype == "bf16" else 4
+    mats = 3 if w.activation == "swiglu" else 2
+    act = int(offsets_active)
+    d, F = w.d, w.F
+    gu_flops = 2.0 * A * d * F * (2 if w.activation == "swiglu" else 1)
+    gu_bytes = act * (mats - 1) * F * d * es + A * d * es + A * F * es
+    dn_flops = 2.0 * A * F * d
+    dn_bytes = act * F * d * es + A * F * es + A * d * 4
+    layer_flops = gu_flops + dn_flops
+    layer_bytes = act * mats * F * d * es + 2 * w.T * d * es + w.N * d * 4
+    return {"gate_up": (gu_flops, gu_bytes), "down": (dn_flops, dn_bytes),
+            "layer": (layer_flops, layer_bytes)}
+
+
+def roofline_entry(flops, nbytes, seconds, peaks, sustained=False):
+    tflops_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    t_tensor = flops / (tflops_peak * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        ach = flops / seconds / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 2), "peak": tflops_peak,
+                "unit": "TFLOP/s", "frac": round(ach / tflops_peak, 4)}
+    ach = nbytes / seconds / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ----------------------------------------------------------------------------
+def host_inputs(w, experts_dev=None):
+    x = moe_inputs.make_x(w)
+    w_r, b_r = moe_inputs.make_router(w)
+    if experts_dev is not None:
+        experts = {k: v.cpu() for k, v in experts_dev.items()}
+    elif torch.cuda.is_available():
+        experts = {k: v.cpu() for k, v in moe_inputs.make_experts(w, "cuda").items()}
+    else:
+        experts = moe_inputs.make_experts(w, "cpu")
+    return x, w_r, b_r, experts
+
+
+def time_oracle(w, x, w_r, b_r, experts, n_tokens):
+    """One call of the oracle as it stands: routing, statistics and dispatch
+    of every token, expert FFN and combine of the first n_tokens tokens."""
+    from oracle import moe_oracle as O
+    t0 = time.perf_counter()
+    O.moe_forward(x, w_r, b_r, lambda e: {k: v[e] for k, v in experts.items()}, K=w.K,
+                  activation=w.activation, capacity_factor=w.capacity_factor, alpha=w.alpha,
+                  add_residual=w.add_residual, tokens=range(n_tokens))
+    return time.perf_counter() - t0
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, experts_dev, budget_s=15.0):
+    x, w_r, b_r, experts = host_inputs(w, experts_dev)
+    n = min(w.T, 64)
+    t = time_oracle(w, x, w_r, b_r, experts, n)
+    # grow the sample towards the time budget (bounded by the workload)
+    while n < w.T and t < budget_s / 4:
+        n = min(w.T, n * 4)
+        t = time_oracle(w, x, w_r, b_r, experts, n)
+    return {"value": round(n / t, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+            "sample": f"float64 oracle: routing/statistics/dispatch of all {w.T} tokens, "
+                      f"experts and combine of the first {n} tokens; {t:.2f} s; "
+                      f"value = {n} tokens / that time"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = moe_inputs.WORKLOADS[args.workload]
+    x, w_r, b_r, experts = host_inputs(w)
+    n = min(w.T, args.ref_tokens)
+    for _ in range(args.warmup):
+        time_oracle(w, x, w_r, b_r, experts, n)
+    times = [time_oracle(w, x, w_r, b_r, experts, n) for _ in range(args.steps)]
+    total = sum(times)
+    value = n * len(times) / total
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, args, extra={"reference_sample_tokens": n}),
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores_used(),
+                             "kind": "oracle",
+                             "sample": f"each step: routing of all {w.T} tokens and experts"
+                                       f" + combine of the first {n} tokens, float64"},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, args, extra=None):
+    cfg = {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.F, "n_experts": w.N,
+           "top_k": w.K, "activation": w.activation, "capacity_factor":
+           (None if math.isinf(w.capacity_factor) else w.capacity_factor),
+           "residual": w.add_residual, "parallelism": f"replicas x{args.gpus}",
+           "l2": "256 MB written before every step, outside the step's event interval; "
+                 "expert weights exceed L2"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, world, rank):
+    import mixture_experts_layer_101_b300 as moe
+
+    moe.load_library()
+    w = moe_inputs.WORKLOADS[args.workload]
+    cfg = moe.LayerConfig.from_workload(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = moe_inputs.make_x(w).to(dev)
+    w_r, b_r = moe_inputs.make_router(w)
+    w_r = w_r.to(dev)
+    b_r = None if b_r is None else b_r.to(dev)
+    experts = moe_inputs.make_experts(w, dev)
+    layer = moe.MoELayer(cfg, w_r, b_r, experts, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    nst = len(moe.TRACE_STAGES) + 1
+    for _ in range(args.warmup):
+        layer.forward(x)
+    torch.cuda.synchronize()
+    layer.stats.status.zero_()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)]
+              for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler() as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            moe.moe_trace_events(events[i])
+            layer.forward(x)
+        moe.moe_trace_events([])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(world)
+
+    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
+    stage_ms = {name: [ev[j].elapsed_time(ev[j + 1]) for ev in events]
+                for j, name in enumerate(moe.TRACE_STAGES)}
+    dev_s = sum(step_ms) / 1e3
+    max_s = max_over_ranks(dev_s, world)
+    tokens = sum_over_ranks(float(w.T * args.steps), world)
+    value = tokens / max_s
+
+    st = layer.stats.to_host()
+    if st["status"] != 0:
+        raise SystemExit(f"device status word {st['status']:#x} after the timed steps")
+    kept = int(st["kept"].sum())
+    active = int((st["kept"] > 0).sum())
+    work = algorithmic_work(w, kept, active)
+    peaks = measured_peaks()
+    gu_s = statistics.mean(stage_ms["ffn_gate_up"]) / 1e3
+    dn_s = statistics.mean(stage_ms["ffn_down"]) / 1e3
+    dominant = "ffn_gate_up" if gu_s >= dn_s else "ffn_down"
+    key = "gate_up" if dominant == "ffn_gate_up" else "down"
+    roof = roofline_entry(*work[key], gu_s if key == "gate_up" else dn_s, peaks)
+    roof["kernel"] = ("grouped_gemm_tc<0> (gate/up + SwiGLU)" if key == "gate_up"
+                      else "grouped_gemm_tc<1> (down)")
+    roof["traffic"] = None
+    roof["peak_source"] = f"{peaks['source']} (burst)"
+    layer_roof = roofline_entry(*work["layer"], statistics.mean(step_ms) / 1e3, peaks)
+
+    # end to end through the public API on host buffers
+    x_host = moe_inputs.make_x(w).pin_memory()
+    y_host = torch.empty((w.T, w.d), dtype=cfg.torch_dtype).pin_memory()
+    e2e_steps = args.steps
+    for _ in range(min(args.warmup, 3)):
+        layer.forward_host(x_host, y_host, x)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        laux = layer.forward_host(x_host, y_host, x)
+        torch.cuda.synchronize()
+        float(laux.item())
+    e2e_s = time.perf_counter() - t0
+    barrier(world)
+    e2e_value = sum_over_ranks(float(w.T * e2e_steps), world) / max_over_ranks(e2e_s, world)
+    es = 2 if w.dtype == "bf16" else 4
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, experts)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * max_s / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": workload_config(w, args),
+            "roofline": roof,
+            "layer_roofline": dict(layer_roof, note="whole step against max(F/peak, B/BW) "
+                                                    "of the layer's algorithmic work"),
+            "stage_ms": {k: round(statistics.mean(v), 4) for k, v in stage_ms.items()},
+            "kept_assignments": kept, "active_experts": active, "n_dropped": st["n_dropped"],
+            "l_aux": st["l_aux"],
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
+                    "h2d_bytes_per_step": w.T * w.d * es,
+                    "d2h_bytes_per_step": w.T * w.d * es + 4},
+            "gpu_launches": 8 * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed_region": round(wall, 4),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mixtral_prefill", choices=sorted(moe_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=256,
+                    help="tokens whose experts the reference arm evaluates per step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("at least 3 warm-up steps")
+    world, rank, _ = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

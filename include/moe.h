@@ -213,6 +213,17 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r,
                        void* y, moe_stats* stats, void* ws,
                        moe_stream_t stream);
 
+/* Tracing (instrumentation; the pages have no counterpart). Registers up to
+ * 6 caller-created CUDA events (cudaEvent_t, passed as void*) for the
+ * calling host thread; n = 0 clears them. While registered, moe_forward
+ * records them on its stream at its stage boundaries:
+ *   events[0] before the router, [1] after the router and statistics,
+ *   [2] after the dispatch, [3] after the gate/up (or first Linear) grouped
+ *   GEMM, [4] after the down grouped GEMM, [5] after the combine.
+ * The library does not own, create or destroy the events.
+ * Errors: MOE_ERR_INVALID (n outside [0, 6], or events NULL with n > 0). */
+moe_status moe_trace_events(void* const* events, int32_t n);
+
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char* moe_status_string(moe_status s);
 

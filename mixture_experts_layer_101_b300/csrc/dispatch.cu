@@ -1,0 +1,154 @@
+// Capacity-limited dispatch: histogram -> prefix scan -> stable permute and
+// gather of the token rows into expert-contiguous order.
+//
+// Source: "MoE 混合专家模型稀疏激活的架构原理与负载均衡挑战" §2.3 (capacity
+// floor(K/N·CF·S); tokens beyond it are dropped and pass on the residual) and
+// §三 MoELayer.forward (outer loop over the top-k rank, tokens in ascending
+// order within it, truncation of each expert's list at the capacity).
+//
+// Visiting order q = k*T + t (rank-major). The grid is (token blocks of 256) x
+// (K ranks); block (b, k) owns the assignments (t in block b, rank k), which
+// are contiguous in q. Rank of an assignment within its expert =
+//   base[k][b][e]  (assignments to e in all earlier (k', b') blocks)
+// + assignments to e in earlier warps of this block
+// + earlier lanes of this warp with the same expert (warp match).
+// Every step is integer and order-defined, so slots are bit-exact.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = kDispatchTokensPerBlock;  // 256 = one token per thread
+
+__global__ void __launch_bounds__(kThreads)
+dispatch_hist_kernel(const int32_t* __restrict__ idx, int T, int K, int N,
+                     int32_t* __restrict__ ghist, uint32_t* status) {
+  __shared__ int32_t hist[256];
+  const int b = blockIdx.x, k = blockIdx.y, nb = gridDim.x;
+  for (int i = threadIdx.x; i < 256; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  const int t = b * kThreads + threadIdx.x;
+  if (t < T) {
+    const int e = idx[static_cast<size_t>(t) * K + k];
+    if (e >= 0 && e < N) atomicAdd(&hist[e], 1);
+    else set_status(status, MOE_ERR_INDEX);
+  }
+  __syncthreads();
+  int32_t* out = ghist + (static_cast<size_t>(k) * nb + b) * N;
+  for (int e = threadIdx.x; e < N; e += kThreads) out[e] = hist[e];
+}
+
+// One block. Thread e scans its expert's column over the K*nb (k, b) blocks
+// in visiting order; then the kept counts are scanned over experts.
+__global__ void __launch_bounds__(256)
+dispatch_scan_kernel(const int32_t* __restrict__ ghist, int nq, int N, int32_t C,
+                     int32_t* __restrict__ gbase, int32_t* __restrict__ offsets,
+                     int32_t* count, int32_t* kept_out, int32_t* n_dropped) {
+  __shared__ int32_t kept[256], cnt[256];
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    int32_t run = 0;
+    for (int q = 0; q < nq; ++q) {
+      gbase[static_cast<size_t>(q) * N + e] = run;
+      run += ghist[static_cast<size_t>(q) * N + e];
+    }
+    cnt[e] = run;
+    kept[e] = run < C ? run : C;
+    if (count) count[e] = run;
+    if (kept_out) kept_out[e] = kept[e];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t off = 0, dropped = 0;
+    for (int e = 0; e < N; ++e) {
+      offsets[e] = off;
+      off += kept[e];
+      dropped += cnt[e] - kept[e];
+    }
+    offsets[N] = off;
+    if (n_dropped) *n_dropped = dropped;
+  }
+}
+
+template <typename Tx>
+__global__ void __launch_bounds__(kThreads)
+dispatch_permute_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ idx, int T, int K,
+                        int N, int d, int32_t C, const int32_t* __restrict__ gbase,
+                        const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_of,
+                        int32_t* __restrict__ token_of_slot, Tx* __restrict__ x_perm) {
+  __shared__ int32_t wcnt[kThreads / 32][256];
+  __shared__ int32_t sslot[kThreads];
+  const int b = blockIdx.x, k = blockIdx.y, nb = gridDim.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < (kThreads / 32) * 256; i += kThreads) (&wcnt[0][0])[i] = 0;
+
+  const int t = b * kThreads + tid;
+  int e = -1;
+  if (t < T) e = idx[static_cast<size_t>(t) * K + k];
+  const bool valid = (t < T) && e >= 0 && e < N;
+  // peers: lanes of this warp routed to the same expert (unique keys otherwise)
+  const int key = valid ? e : N + lane;
+  const uint32_t peers = __match_any_sync(0xffffffffu, key);
+  const uint32_t lower = peers & ((1u << lane) - 1u);
+  const int rank_w = __popc(lower);
+  __syncthreads();
+  if (valid && rank_w == 0) wcnt[warp][e] = __popc(peers);
+  __syncthreads();
+
+  int32_t slot = -1;
+  if (valid) {
+    int32_t rank = gbase[(static_cast<size_t>(k) * nb + b) * N + e] + rank_w;
+    for (int w = 0; w < warp; ++w) rank += wcnt[w][e];
+    if (rank < C) {
+      slot = offsets[e] + rank;
+      token_of_slot[slot] = t;
+    }
+  }
+  if (t < T) slot_of[static_cast<size_t>(t) * K + k] = slot;
+  sslot[tid] = slot;
+  __syncthreads();
+
+  // gather: each warp copies the rows of its 32 assignments, 16 bytes a lane
+  const int chunks = d * static_cast<int>(sizeof(Tx)) / 16;
+  for (int i = 0; i < 32; ++i) {
+    const int s = sslot[warp * 32 + i];
+    if (s < 0) continue;
+    const int tt = b * kThreads + warp * 32 + i;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(tt) * d);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(s) * d);
+    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+}  // namespace
+
+moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* idx,
+                           int32_t* offsets, int32_t* slot_of, int32_t* token_of_slot,
+                           void* x_perm, int32_t* ghist, int32_t* gbase, const moe_stats* st,
+                           cudaStream_t s) {
+  const int N = c.n_experts, K = c.top_k;
+  const int32_t C = capacity_of(&c);
+  uint32_t* status = st ? st->status : nullptr;
+  const int nb = (c.T + kThreads - 1) / kThreads;
+  if (c.T > 0) {
+    dispatch_hist_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, ghist, status);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  dispatch_scan_kernel<<<1, 256, 0, s>>>(ghist, c.T > 0 ? K * nb : 0, N, C, gbase, offsets,
+                                         st ? st->count : nullptr, st ? st->kept : nullptr,
+                                         st ? st->n_dropped : nullptr);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (c.T > 0) {
+    if (c.dtype == MOE_BF16)
+      dispatch_permute_kernel<__nv_bfloat16><<<dim3(nb, K), kThreads, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(x), idx, c.T, K, N, c.d_model, C, gbase, offsets,
+          slot_of, token_of_slot, static_cast<__nv_bfloat16*>(x_perm));
+    else
+      dispatch_permute_kernel<float><<<dim3(nb, K), kThreads, 0, s>>>(
+          static_cast<const float*>(x), idx, c.T, K, N, c.d_model, C, gbase, offsets, slot_of,
+          token_of_slot, static_cast<float*>(x_perm));
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,415 @@
+// Grouped expert FFN on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// Sources: "MoE 混合专家模型稀疏激活的架构原理与负载均衡挑战" §三 class Expert
+// (down(silu(gate(x)) * up(x))) and its note in MoELayer.forward that the
+// per-expert loop should become a grouped matrix multiply in production.
+//
+// Two launches of one persistent, warp-specialised kernel:
+//   gate/up:  h[s, n] = silu(x_perm[s] . W_gate[e, n]) * (x_perm[s] . W_up[e, n])
+//             output tile 128 rows x 128 columns of h; the MMA's B operand is
+//             128 rows of W_gate followed by the same 128 rows of W_up, so one
+//             M=128, N=256 MMA produces both halves side by side in TMEM and
+//             the SwiGLU is applied in the epilogue (h rounded to bf16 once).
+//   down:     o[s, n] = h[s] . W_down[e, n], tile 128 x 256, fp32 output.
+// The rows s of expert e are the contiguous slots [offsets[e], offsets[e+1])
+// written by the dispatch; a 128-row tile may run past its expert's last
+// slot: those rows are computed from whatever follows and never stored (rows
+// of D depend only on the same rows of A).
+//
+// Per CTA (one per SM, 192 threads):
+//   warp 0      TMA producer: A and B tiles (128-byte swizzle, 64 bf16 of K
+//               per row) into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma (M=128,
+//               N=256, K=16; four per 64-wide stage) into one of two fp32
+//               accumulators (256 columns each), committing each stage back
+//               to the producer and each finished tile to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, activation,
+//               stores; the second accumulator lets tile i's epilogue overlap
+//               tile i+1's main loop.
+// Tiles are (expert, n-tile, m-tile) with m fastest, dealt round-robin over
+// the CTAs, so CTAs running at the same time share weight tiles through L2.
+// Every wait is bounded (1 s of wall time); on expiry the block records
+// MOE_ERR_TIMEOUT in the status word, lets its copies and MMAs drain,
+// frees its TMEM and returns.
+#include "moe_common.cuh"
+#include "ptx_sm100.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BK = 64, STAGES = 4, kThreads = 192;
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B_BYTES = 256 * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = 256;           // fp32 accumulator 128 x 256
+constexpr int TMEM_COLS = 512;          // two accumulators
+constexpr int MAX_EXPERTS = 256;
+constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
+                           2 * (MAX_EXPERTS + 1) * 4;
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, 256);
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+struct TcArgs {
+  const int32_t* offsets;  // [N+1] slot offsets of the experts
+  int n_experts;
+  int kdim;                // reduction length: d (gate/up) or F (down)
+  int n_tiles;             // output tiles per expert: F/128 (gate/up) or d/256 (down)
+  int b_rows;              // rows of B per expert: F (gate/up) or d (down)
+  void* out;               // h (bf16, row length F) or o (fp32, row length d)
+  int ldo;
+  uint32_t* status;
+};
+
+// MODE 0: gate/up + SwiGLU -> h (bf16). MODE 1: down -> o (fp32).
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+  using namespace ptx;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base, sB = base + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
+  int* seg_off = tile_start + (MAX_EXPERTS + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = args.n_experts;
+  const int KB = args.kdim / BK;
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto bar_tfull = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
+  auto bar_tempty = [&](int a) { return smem_u32(bars + 2 * STAGES + 2 + a); };
+  const uint32_t bar_drain = smem_u32(bars + 2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull(a), 1);
+      mbar_init(bar_tempty(a), 4);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    if (MODE == 0) prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    // tile_start[e] = tiles of experts < e; lane owns experts [8*lane, 8*lane+8)
+    constexpr int PER = MAX_EXPERTS / 32;
+    int local[PER], sum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane * PER + j;
+      int tiles = 0;
+      if (e < N) {
+        const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
+        seg_off[e] = o0;
+        tiles = ((o1 - o0 + BM - 1) / BM) * args.n_tiles;
+      }
+      local[j] = tiles;
+      sum += tiles;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane * PER + j;
+      if (e < N) tile_start[e] = run;
+      run += local[j];
+    }
+    if (lane == 31) tile_start[N] = incl;
+    if (lane == 0) seg_off[N] = args.offsets[N];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tile_start[N];
+
+  auto decode = [&](int tile, int& e, int& m, int& n) {
+    int lo = 0, hi = N - 1;  // last expert whose first tile is <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    e = lo;
+    const int mt = (seg_off[e + 1] - seg_off[e] + BM - 1) / BM;
+    const int local = tile - tile_start[e];
+    n = local / mt;
+    m = local - n * mt;
+  };
+  auto fail = [&]() {
+    set_status(args.status, MOE_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer ----
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_parity = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, m, n;
+      decode(tile, e, m, n);
+      const int row_a = seg_off[e] + m * BM;
+      const int row_b = e * args.b_rows + n * (MODE == 0 ? 128 : 256);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(bar_empty(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_full(stage), STAGE_BYTES);
+        const uint32_t a_dst = sA + stage * A_BYTES, b_dst = sB + stage * B_BYTES;
+        tma_load_2d(a_dst, &tmA, bar_full(stage), kb * BK, row_a);
+        if (MODE == 0) {
+          tma_load_2d(b_dst, &tmB0, bar_full(stage), kb * BK, row_b);
+          tma_load_2d(b_dst + B_BYTES / 2, &tmB1, bar_full(stage), kb * BK, row_b);
+        } else {
+          tma_load_2d(b_dst, &tmB0, bar_full(stage), kb * BK, row_b);
+        }
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      fail();
+      // let the copies already in flight land before the block exits
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s)) mbar_wait(bar_full(s), (issued_parity >> s) & 1u, kWaitLimitNs, nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer ----
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued_any = false;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(bar_full(stage), phase, kWaitLimitNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * B_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32), sdesc_kmajor_sw128(b0 + kk * 32),
+                   IDESC, (kb | kk) != 0 ? 1u : 0u);
+        issued_any = true;
+        mma_commit(bar_empty(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit(bar_tfull(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      fail();
+      if (issued_any) {  // wait for the MMAs in flight before TMEM is freed
+        mma_commit(bar_drain);
+        mbar_wait(bar_drain, 0, kWaitLimitNs, nullptr);
+      }
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue ----
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, m, n;
+      decode(tile, e, m, n);
+      const int cnt = seg_off[e + 1] - seg_off[e];
+      bool ok = mbar_wait(bar_tfull(acc), acc_phase, kWaitLimitNs, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const int r = m * BM + q * 32 + lane;
+      const bool valid = r < cnt;
+      const size_t grow = static_cast<size_t>(seg_off[e]) + static_cast<size_t>(r);
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * ACC_COLS) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+      if (MODE == 0) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo + n * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + 128 + c * 32, u);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+            const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+            const float h0 = g0 / (1.f + __expf(-g0)) * u0;
+            const float h1 = g1 / (1.f + __expf(-g1)) * u1;
+            __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+            packed[j] = *reinterpret_cast<uint32_t*>(&hb);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                  packed[4 * v + 3]);
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(args.out) + grow * args.ldo + n * 256;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(out + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] as a 2-D tensor map with a box of
+// box_rows x 64 columns and the 128-byte swizzle; out-of-range rows read 0.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool set_smem_attr() {
+  // Per device; the attribute is cheap to set, so set it on every device once.
+  static int done_mask = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 31 && (done_mask >> dev) & 1) return true;
+  if (cudaFuncSetAttribute(grouped_gemm_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES) != cudaSuccess ||
+      cudaFuncSetAttribute(grouped_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES) != cudaSuccess)
+    return false;
+  if (dev < 31) done_mask |= 1 << dev;
+  return true;
+}
+
+}  // namespace
+
+bool ffn_tc_supported(const moe_config& c) {
+  return c.dtype == MOE_BF16 && c.activation == MOE_SWIGLU && c.d_model % 256 == 0 &&
+         c.d_ff % 128 == 0 && c.n_experts <= MAX_EXPERTS;
+}
+
+moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
+                         const int32_t* offsets, const moe_expert_weights& w, void* h, float* o,
+                         uint32_t* status, cudaStream_t s, int part) {
+  if (a_max == 0) return MOE_OK;
+  const int N = c.n_experts, d = c.d_model, F = c.d_ff;
+  CUtensorMap mx, mg, mu, mh, md;
+  if (!make_map(&mx, x_perm, a_max, d, 128) ||
+      !make_map(&mg, w.w_gate, static_cast<uint64_t>(N) * F, d, 128) ||
+      !make_map(&mu, w.w_up, static_cast<uint64_t>(N) * F, d, 128) ||
+      !make_map(&mh, h, a_max, F, 128) ||
+      !make_map(&md, w.w_down, static_cast<uint64_t>(N) * d, F, 256))
+    return MOE_ERR_CUDA;
+  if (!set_smem_attr()) return MOE_ERR_CUDA;
+  const int64_t mtiles = N + (a_max + BM - 1) / BM;  // upper bound on (expert, m-tile) pairs
+  const int sms = sm_count();
+  if (part & 1) {
+    TcArgs a1{offsets, N, d, F / 128, F, h, F, status};
+    const int64_t t1 = mtiles * (F / 128);
+    grouped_gemm_tc<0><<<static_cast<unsigned>(t1 < sms ? t1 : sms), kThreads, SMEM_BYTES, s>>>(
+        mx, mg, mu, a1);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (part & 2) {
+    TcArgs a2{offsets, N, F, d / 256, d, o, d, status};
+    const int64_t t2 = mtiles * (d / 256);
+    grouped_gemm_tc<1><<<static_cast<unsigned>(t2 < sms ? t2 : sms), kThreads, SMEM_BYTES, s>>>(
+        mh, md, md, a2);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

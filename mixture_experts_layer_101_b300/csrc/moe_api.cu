@@ -1,0 +1,316 @@
+// C ABI of libmoe (declared in include/moe.h): argument checks, the
+// workspace layout, and the order of launches. All compute is in the
+// kernels of router.cu, dispatch.cu, ffn_tc.cu, ffn_simt.cu and combine.cu.
+#include "moe_common.cuh"
+
+#include <math.h>
+
+#include <mutex>
+
+namespace moe {
+
+namespace {
+constexpr int64_t kMaxT = int64_t(1) << 24;
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int dtype_size(const moe_config* c) { return c->dtype == MOE_BF16 ? 2 : 4; }
+}  // namespace
+
+bool config_valid(const moe_config* c, moe_status* why) {
+  auto bad = [&](moe_status s) {
+    if (why) *why = s;
+    return false;
+  };
+  if (!c) return bad(MOE_ERR_INVALID);
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return bad(MOE_ERR_INVALID);
+  if (c->activation != MOE_SWIGLU && c->activation != MOE_GELU) return bad(MOE_ERR_INVALID);
+  if ((c->has_bias != 0 && c->has_bias != 1) || (c->add_residual != 0 && c->add_residual != 1))
+    return bad(MOE_ERR_INVALID);
+  if (c->T < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0)
+    return bad(MOE_ERR_INVALID);
+  if (c->top_k > c->n_experts) return bad(MOE_ERR_INVALID);
+  if (isnan(c->capacity_factor) || !isfinite(c->alpha)) return bad(MOE_ERR_INVALID);
+  if (c->T > kMaxT || c->n_experts > 256 || c->top_k > 8) return bad(MOE_ERR_UNSUPPORTED);
+  if (c->d_model % (c->dtype == MOE_BF16 ? 8 : 4) != 0 || c->d_ff % 4 != 0)
+    return bad(MOE_ERR_UNSUPPORTED);
+  if (c->has_bias && c->activation != MOE_GELU) return bad(MOE_ERR_UNSUPPORTED);
+  return true;
+}
+
+// floor(K * CF * T / N) on the exact value of the float CF. K*CF*T is exact
+// in double (a 24-bit significand times an integer below 2^27); the quotient
+// is then corrected against exact integer products.
+int32_t capacity_of(const moe_config* c) {
+  const double cf = static_cast<double>(c->capacity_factor);
+  if (!(cf > 0.0) || isinf(cf)) return INT32_MAX;
+  const double q = static_cast<double>(c->top_k) * cf * static_cast<double>(c->T);
+  const double n = static_cast<double>(c->n_experts);
+  double f = floor(q / n);
+  while ((f + 1.0) * n <= q) f += 1.0;
+  while (f > 0.0 && f * n > q) f -= 1.0;
+  return f >= static_cast<double>(INT32_MAX) ? INT32_MAX : static_cast<int32_t>(f);
+}
+
+int64_t a_max_of(const moe_config* c) {
+  const int64_t tk = static_cast<int64_t>(c->T) * c->top_k;
+  const int64_t nc = static_cast<int64_t>(c->n_experts) * capacity_of(c);
+  return tk < nc ? tk : nc;
+}
+
+WsLayout ws_layout(const moe_config* c) {
+  WsLayout L{};
+  size_t total = 0;
+  auto take = [&](size_t bytes) {
+    const size_t off = total;
+    total += align256(bytes);
+    return off;
+  };
+  const size_t T = static_cast<size_t>(c->T), K = c->top_k, N = c->n_experts;
+  const size_t d = c->d_model, F = c->d_ff, es = dtype_size(c);
+  L.a_max = a_max_of(c);
+  L.nblk_r = static_cast<int>((T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock);
+  L.nblk_d = static_cast<int>((T + kDispatchTokensPerBlock - 1) / kDispatchTokensPerBlock);
+  const size_t nr = L.nblk_r > 0 ? L.nblk_r : 1, nd = L.nblk_d > 0 ? L.nblk_d : 1;
+  const size_t A = static_cast<size_t>(L.a_max);
+  L.idx = take(T * K * 4);
+  L.gate = take(T * K * 4);
+  L.psum = take(nr * N * 4);
+  L.pcnt = take(nr * N * 4);
+  L.ghist = take(K * nd * N * 4);
+  L.gbase = take(K * nd * N * 4);
+  L.offsets = take((N + 1) * 4);
+  L.slot_of = take(T * K * 4);
+  L.token_of_slot = take((A > 0 ? A : 1) * 4);
+  L.x_perm = take(A * d * es);
+  L.h = take(A * F * es);
+  L.o = take(A * d * 4);
+  L.total = total;
+  return L;
+}
+
+int sm_count() {
+  static int counts[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && counts[dev] > 0) return counts[dev];
+  int n = 148;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) counts[dev] = n;
+  return n;
+}
+
+namespace {
+
+moe_status check_ws(const moe_config* c, const void* ws) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  (void)c;
+  return MOE_OK;
+}
+
+uint8_t* at(void* ws, size_t off) {
+  return static_cast<uint8_t*>(ws) + off;
+}
+
+moe_status check_weights(const moe_config* c, const moe_expert_weights* w) {
+  if (!w) return MOE_ERR_INVALID;
+  if (c->activation == MOE_SWIGLU) {
+    if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID;
+    if (!aligned16(w->w_gate) || !aligned16(w->w_up) || !aligned16(w->w_down))
+      return MOE_ERR_INVALID;
+  } else {
+    if (!w->w1 || !w->w2) return MOE_ERR_INVALID;
+    if (c->has_bias && (!w->b1 || !w->b2)) return MOE_ERR_INVALID;
+    if (!aligned16(w->w1) || !aligned16(w->w2)) return MOE_ERR_INVALID;
+  }
+  return MOE_OK;
+}
+
+// Per-thread trace: events recorded on the launch stream at the stage
+// boundaries of moe_forward (see moe_trace_events).
+constexpr int kMaxTrace = 6;
+thread_local cudaEvent_t g_trace[kMaxTrace] = {};
+thread_local int g_ntrace = 0;
+
+void trace(int i, cudaStream_t s) {
+  if (i < g_ntrace && g_trace[i] != nullptr) cudaEventRecord(g_trace[i], s);
+}
+
+moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offsets,
+                    const moe_expert_weights* w, float* o, moe_stats* stats, void* ws,
+                    cudaStream_t s, bool traced) {
+  const WsLayout L = ws_layout(c);
+  void* h = at(ws, L.h);
+  const bool tc = ffn_tc_supported(*c);
+  uint32_t* status = stats ? stats->status : nullptr;
+  for (int part = 1; part <= 2; ++part) {
+    const moe_status r = tc ? launch_ffn_tc(*c, L.a_max, x_perm, offsets, *w, h, o, status, s, part)
+                            : launch_ffn_simt(*c, L.a_max, x_perm, offsets, *w, h, o, s, part);
+    if (r != MOE_OK) return r;
+    if (traced) trace(2 + part, s);
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config* cfg) {
+  if (!config_valid(cfg, nullptr)) return 0;
+  return ws_layout(cfg).total;
+}
+
+int32_t moe_capacity(const moe_config* cfg) {
+  if (!config_valid(cfg, nullptr)) return -1;
+  return capacity_of(cfg);
+}
+
+int32_t moe_ffn_uses_tensor_cores(const moe_config* cfg) {
+  if (!config_valid(cfg, nullptr)) return -1;
+  return ffn_tc_supported(*cfg) ? 1 : 0;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_NONFINITE: return "non-finite router logit";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_INDEX: return "expert index out of range";
+  }
+  return "unknown status";
+}
+
+moe_status moe_trace_events(void* const* events, int32_t n) {
+  if (n < 0 || n > kMaxTrace || (n > 0 && events == nullptr)) return MOE_ERR_INVALID;
+  for (int i = 0; i < kMaxTrace; ++i)
+    g_trace[i] = i < n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  g_ntrace = n;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r, const float* b_r,
+                     int32_t* idx, float* gate, moe_stats* stats, void* ws, moe_stream_t stream) {
+  try {
+    moe_status why = MOE_OK;
+    if (!config_valid(cfg, &why)) return why;
+    if (!x || !w_r || !idx || !gate) return MOE_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w_r) || !aligned16(idx) || !aligned16(gate) ||
+        (b_r && !aligned16(b_r)))
+      return MOE_ERR_INVALID;
+    if (moe_status s = check_ws(cfg, ws)) return s;
+    const WsLayout L = ws_layout(cfg);
+    return launch_router(*cfg, x, w_r, b_r, idx, gate, reinterpret_cast<float*>(at(ws, L.psum)),
+                         reinterpret_cast<int32_t*>(at(ws, L.pcnt)), stats,
+                         static_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return MOE_ERR_CUDA;
+  }
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* idx, int32_t* offsets,
+                        int32_t* slot_of, int32_t* token_of_slot, void* x_perm, moe_stats* stats,
+                        void* ws, moe_stream_t stream) {
+  try {
+    moe_status why = MOE_OK;
+    if (!config_valid(cfg, &why)) return why;
+    if (!x || !idx || !offsets || !slot_of || !token_of_slot || !x_perm) return MOE_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(idx) || !aligned16(offsets) || !aligned16(slot_of) ||
+        !aligned16(token_of_slot) || !aligned16(x_perm))
+      return MOE_ERR_INVALID;
+    if (moe_status s = check_ws(cfg, ws)) return s;
+    const WsLayout L = ws_layout(cfg);
+    return launch_dispatch(*cfg, x, idx, offsets, slot_of, token_of_slot, x_perm,
+                           reinterpret_cast<int32_t*>(at(ws, L.ghist)),
+                           reinterpret_cast<int32_t*>(at(ws, L.gbase)), stats,
+                           static_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return MOE_ERR_CUDA;
+  }
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                          const moe_expert_weights* weights, float* o, moe_stats* stats, void* ws,
+                          moe_stream_t stream) {
+  try {
+    moe_status why = MOE_OK;
+    if (!config_valid(cfg, &why)) return why;
+    if (!x_perm || !offsets || !o) return MOE_ERR_INVALID;
+    if (!aligned16(x_perm) || !aligned16(offsets) || !aligned16(o)) return MOE_ERR_INVALID;
+    if (moe_status s = check_weights(cfg, weights)) return s;
+    if (moe_status s = check_ws(cfg, ws)) return s;
+    return ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws,
+                    static_cast<cudaStream_t>(stream), false);
+  } catch (...) {
+    return MOE_ERR_CUDA;
+  }
+}
+
+moe_status moe_combine(const moe_config* cfg, const float* o, const int32_t* slot_of,
+                       const float* gate, const void* x, void* y, moe_stream_t stream) {
+  try {
+    moe_status why = MOE_OK;
+    if (!config_valid(cfg, &why)) return why;
+    if (!o || !slot_of || !gate || !y || (cfg->add_residual && !x)) return MOE_ERR_INVALID;
+    if (!aligned16(o) || !aligned16(slot_of) || !aligned16(gate) || !aligned16(y) ||
+        (x && !aligned16(x)))
+      return MOE_ERR_INVALID;
+    return launch_combine(*cfg, o, slot_of, gate, x, y, static_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return MOE_ERR_CUDA;
+  }
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r, const float* b_r,
+                       const moe_expert_weights* weights, void* y, moe_stats* stats, void* ws,
+                       moe_stream_t stream) {
+  try {
+    moe_status why = MOE_OK;
+    if (!config_valid(cfg, &why)) return why;
+    if (!x || !w_r || !y) return MOE_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w_r) || !aligned16(y) || (b_r && !aligned16(b_r)))
+      return MOE_ERR_INVALID;
+    if (moe_status s = check_weights(cfg, weights)) return s;
+    if (moe_status s = check_ws(cfg, ws)) return s;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(cfg);
+    int32_t* idx = reinterpret_cast<int32_t*>(at(ws, L.idx));
+    float* gate = reinterpret_cast<float*>(at(ws, L.gate));
+    int32_t* offsets = reinterpret_cast<int32_t*>(at(ws, L.offsets));
+    int32_t* slot_of = reinterpret_cast<int32_t*>(at(ws, L.slot_of));
+    int32_t* tos = reinterpret_cast<int32_t*>(at(ws, L.token_of_slot));
+    void* x_perm = at(ws, L.x_perm);
+    float* o = reinterpret_cast<float*>(at(ws, L.o));
+    trace(0, s);
+    moe_status r = launch_router(*cfg, x, w_r, b_r, idx, gate,
+                                 reinterpret_cast<float*>(at(ws, L.psum)),
+                                 reinterpret_cast<int32_t*>(at(ws, L.pcnt)), stats, s);
+    if (r != MOE_OK) return r;
+    trace(1, s);
+    r = launch_dispatch(*cfg, x, idx, offsets, slot_of, tos, x_perm,
+                        reinterpret_cast<int32_t*>(at(ws, L.ghist)),
+                        reinterpret_cast<int32_t*>(at(ws, L.gbase)), stats, s);
+    if (r != MOE_OK) return r;
+    trace(2, s);
+    r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true);
+    if (r != MOE_OK) return r;
+    r = launch_combine(*cfg, o, slot_of, gate, x, y, s);
+    trace(5, s);
+    return r;
+  } catch (...) {
+    return MOE_ERR_CUDA;
+  }
+}
+
+}  // extern "C"

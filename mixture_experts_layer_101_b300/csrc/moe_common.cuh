@@ -1,0 +1,103 @@
+// Internal declarations shared by the translation units of libmoe.
+// Not part of the public ABI (that is include/moe.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---- device helpers --------------------------------------------------------
+__device__ __forceinline__ void set_status(uint32_t* status, moe_status code) {
+  if (status) atomicOr(status, 1u << static_cast<uint32_t>(code));
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// Load 4 consecutive elements (16-byte aligned for fp32, 8-byte for bf16).
+__device__ __forceinline__ float4 load4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x);
+  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+  float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+__device__ __forceinline__ void store4(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// ---- workspace layout ------------------------------------------------------
+// Every region is 256-byte aligned. The same layout serves every entry point;
+// moe_workspace_size() returns its total.
+constexpr int kRouterTokensPerBlock = 32;   // tokens per router block
+constexpr int kDispatchTokensPerBlock = 256; // tokens per dispatch block
+
+struct WsLayout {
+  size_t idx, gate;           // [T][K] int32 / fp32 (moe_forward only)
+  size_t psum, pcnt;          // router partials [nblk_r][N]
+  size_t ghist, gbase;        // dispatch histograms [K][nblk_d][N]
+  size_t offsets;             // [N+1] (moe_forward only)
+  size_t slot_of;             // [T][K] (moe_forward only)
+  size_t token_of_slot;       // [A_max] (moe_forward only)
+  size_t x_perm;              // [A_max][d] dtype (moe_forward only)
+  size_t h;                   // [A_max][F] dtype
+  size_t o;                   // [A_max][d] fp32 (moe_forward only)
+  size_t total;
+  int64_t a_max;
+  int nblk_r, nblk_d;
+};
+
+// Host-side helpers implemented in moe_api.cu.
+bool config_valid(const moe_config* c, moe_status* why);
+int32_t capacity_of(const moe_config* c);
+int64_t a_max_of(const moe_config* c);
+WsLayout ws_layout(const moe_config* c);
+int sm_count();
+
+// ---- launchers (each returns MOE_OK or MOE_ERR_CUDA) -----------------------
+moe_status launch_router(const moe_config& c, const void* x, const float* w_r,
+                         const float* b_r, int32_t* idx, float* gate, float* psum,
+                         int32_t* pcnt, const moe_stats* st, cudaStream_t s);
+
+moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* idx,
+                           int32_t* offsets, int32_t* slot_of, int32_t* token_of_slot,
+                           void* x_perm, int32_t* ghist, int32_t* gbase,
+                           const moe_stats* st, cudaStream_t s);
+
+moe_status launch_combine(const moe_config& c, const float* o, const int32_t* slot_of,
+                          const float* gate, const void* x, void* y, cudaStream_t s);
+
+// Expert FFN on CUDA cores (any dtype/shape). part: 1 = gate/up (or the
+// first Linear + GELU) into h, 2 = down projection into o, 3 = both.
+moe_status launch_ffn_simt(const moe_config& c, int64_t a_max, const void* x_perm,
+                           const int32_t* offsets, const moe_expert_weights& w,
+                           void* h, float* o, cudaStream_t s, int part);
+
+// Expert FFN on tcgen05 tensor cores (bf16, d % 256 == 0, F % 128 == 0).
+bool ffn_tc_supported(const moe_config& c);
+moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
+                         const int32_t* offsets, const moe_expert_weights& w,
+                         void* h, float* o, uint32_t* status, cudaStream_t s, int part);
+
+}  // namespace moe

@@ -1,0 +1,283 @@
+// Fused router: logits = x W_r^T (+ b_r), softmax, top-K, renormalised gates,
+// and per-block partial sums of the load-balance statistics; then a one-block
+// kernel reduces the partials in a fixed order into count, f, P and L_aux.
+//
+// Sources: "MoE 混合专家模型稀疏激活的架构原理与负载均衡挑战" §2.1 (logits =
+// x·W_r, Top-K, softmax over the selected logits) and §2.2 (L_aux =
+// alpha·N·Σ f_i·P_i, f from the top-k indices, P the mean router probability);
+// "混合专家模型（Mixture of Experts, MoE）" 结构 2 (G(x) = Softmax(W_r·x)) and
+// 运行示例 (router = nn.Linear with bias; renormalised top-K weights).
+//
+// Design: one block of 256 threads owns 32 tokens and all N experts. The 8
+// warps split the work (experts x d-slices) so that every N in [1, 256] keeps
+// all warps busy; the d-slices are summed in shared memory in a fixed order
+// (deterministic), the logits of the block's 32 tokens then sit in shared
+// memory and each warp runs softmax / top-K / gates for 4 tokens with warp
+// shuffles. The contraction runs in fp32 FFMA (tf32 tensor cores would not
+// keep the logits accurate enough for bit-exact routing against float64).
+#include "moe_common.cuh"
+
+#include <float.h>
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int BM = kRouterTokensPerBlock;  // 32 tokens per block
+
+// NPW: experts per warp (8: N <= 8, one token per lane; 32: 4 tokens x 8
+// experts per lane). WS_N: warps across experts; the other 8/WS_N warps split d.
+template <typename Tx, int NPW, int WS_N>
+__global__ void __launch_bounds__(kThreads)
+router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
+              const float* __restrict__ b_r, int T, int d, int N, int K,
+              int32_t* __restrict__ idx_out, float* __restrict__ gate_out,
+              float* __restrict__ psum, int32_t* __restrict__ pcnt,
+              uint32_t* __restrict__ status) {
+  constexpr int WS_K = kWarps / WS_N;
+  constexpr int NP = NPW * WS_N;                  // padded expert count
+  constexpr int LT = (NPW == 8) ? 32 : 8;         // lanes across tokens
+  constexpr int LE = 32 / LT;                     // lanes across experts
+  constexpr int TT = BM / LT;                     // tokens per lane
+  constexpr int TE = NPW / LE;                    // experts per lane (8)
+  static_assert(TT * LT == BM && TE * LE == NPW, "tile shape");
+
+  __shared__ float red[WS_K * BM * NP];           // partial logits per d-slice
+  __shared__ float pw[kWarps][256];               // per-warp probability sums
+  __shared__ int32_t scnt[256];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * BM;
+  const int wn = warp % WS_N, wk = warp / WS_N;
+  const int lt = lane / LE, le = lane % LE;
+
+  for (int i = tid; i < 256; i += kThreads) scnt[i] = 0;
+
+  // ---- phase A: partial logits over this warp's d-slice ----
+  float acc[TT][TE];
+#pragma unroll
+  for (int i = 0; i < TT; ++i)
+#pragma unroll
+    for (int j = 0; j < TE; ++j) acc[i][j] = 0.f;
+
+  const int slice = ((d / 4 + WS_K - 1) / WS_K) * 4;
+  const int kb = min(d, wk * slice), ke = min(d, kb + slice);
+  const Tx* xrow[TT];
+  bool tok_ok[TT];
+#pragma unroll
+  for (int i = 0; i < TT; ++i) {
+    const int t = t0 + lt * TT + i;
+    tok_ok[i] = t < T;
+    xrow[i] = x + static_cast<size_t>(tok_ok[i] ? t : 0) * d;
+  }
+  const float* wrow[TE];
+  bool exp_ok[TE];
+#pragma unroll
+  for (int j = 0; j < TE; ++j) {
+    const int e = wn * NPW + le * TE + j;
+    exp_ok[j] = e < N;
+    wrow[j] = w_r + static_cast<size_t>(exp_ok[j] ? e : 0) * d;
+  }
+  for (int k = kb; k < ke; k += 4) {
+    float4 xv[TT], wv[TE];
+#pragma unroll
+    for (int i = 0; i < TT; ++i) xv[i] = load4(xrow[i] + k);
+#pragma unroll
+    for (int j = 0; j < TE; ++j) wv[j] = load4(wrow[j] + k);
+#pragma unroll
+    for (int i = 0; i < TT; ++i)
+#pragma unroll
+      for (int j = 0; j < TE; ++j) {
+        float a = acc[i][j];
+        a = fmaf(xv[i].x, wv[j].x, a);
+        a = fmaf(xv[i].y, wv[j].y, a);
+        a = fmaf(xv[i].z, wv[j].z, a);
+        a = fmaf(xv[i].w, wv[j].w, a);
+        acc[i][j] = a;
+      }
+  }
+#pragma unroll
+  for (int i = 0; i < TT; ++i)
+#pragma unroll
+    for (int j = 0; j < TE; ++j)
+      red[(wk * BM + lt * TT + i) * NP + wn * NPW + le * TE + j] = acc[i][j];
+  __syncthreads();
+
+  // ---- phase B: sum the d-slices in a fixed order, add the bias ----
+  for (int i = tid; i < BM * NP; i += kThreads) {
+    float s = red[i];
+#pragma unroll
+    for (int q = 1; q < WS_K; ++q) s += red[q * BM * NP + i];
+    const int e = i % NP;
+    if (b_r != nullptr && e < N) s += b_r[e];
+    red[i] = s;
+  }
+  __syncthreads();
+
+  // ---- phase C: softmax, top-K and gates; warp per token ----
+  constexpr int NJ = (NP + 31) / 32;  // experts per lane in this phase
+  float pacc[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) pacc[j] = 0.f;
+
+  for (int tl = warp; tl < BM; tl += kWarps) {
+    const int t = t0 + tl;
+    if (t >= T) break;
+    float v[NJ];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = (e < N) ? red[tl * NP + e] : -INFINITY;
+      if (e < N && !isfinite(v[j])) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+    // softmax over the N experts
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) m = fmaxf(m, v[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float p[NJ], s = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      p[j] = (lane + 32 * j < N) ? expf(v[j] - m) : 0.f;
+      s += p[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float inv = 1.f / s;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) pacc[j] += p[j] * inv;
+
+    // top-K: K rounds of a warp arg-max (largest logit, then lower index)
+    uint32_t taken = 0;
+    float sel_v = 0.f;
+    int sel_e = 0;
+    float top_v = 0.f, gsum = 0.f;
+    for (int k = 0; k < K; ++k) {
+      float bv = -INFINITY;
+      int be = INT32_MAX;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int e = lane + 32 * j;
+        const float vv = isnan(v[j]) ? -INFINITY : v[j];
+        if (e < N && !(taken & (1u << j)) && (vv > bv || (vv == bv && e < be))) {
+          bv = vv;
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if (be < 0 || be >= N) be = 0;  // unreachable while K <= N; keeps indices in range
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (k == 0) top_v = bv;
+      const float g = expf(bv - top_v);
+      gsum += g;
+      if (lane == k) {
+        sel_v = g;
+        sel_e = be;
+      }
+    }
+    if (lane < K) {
+      idx_out[static_cast<size_t>(t) * K + lane] = sel_e;
+      gate_out[static_cast<size_t>(t) * K + lane] = sel_v / gsum;
+      atomicAdd(&scnt[sel_e], 1);
+    }
+  }
+
+  // ---- phase D: per-block partials in a fixed order ----
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if (lane + 32 * j < 256) pw[warp][lane + 32 * j] = pacc[j];
+  __syncthreads();
+  for (int e = tid; e < N; e += kThreads) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += pw[w][e];
+    psum[static_cast<size_t>(blockIdx.x) * N + e] = s;
+    pcnt[static_cast<size_t>(blockIdx.x) * N + e] = scnt[e];
+  }
+}
+
+// One block: count[e], P[e] = (1/T) sum_b psum[b][e] (b ascending),
+// f[e] = count/(T*K), L_aux = alpha*N*sum_e f[e]*P[e] (e ascending).
+__global__ void __launch_bounds__(256)
+route_stats_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pcnt, int nblk,
+                   int T, int N, int K, float alpha, int32_t* count, float* f, float* P,
+                   float* l_aux) {
+  __shared__ float fp[256];
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    float s = 0.f;
+    int32_t c = 0;
+    for (int b = 0; b < nblk; ++b) {
+      s += psum[static_cast<size_t>(b) * N + e];
+      c += pcnt[static_cast<size_t>(b) * N + e];
+    }
+    const float Pe = T > 0 ? s / static_cast<float>(T) : 0.f;
+    const float fe = T > 0 ? static_cast<float>(c) / (static_cast<float>(T) * K) : 0.f;
+    if (count) count[e] = c;
+    if (f) f[e] = fe;
+    if (P) P[e] = Pe;
+    fp[e] = fe * Pe;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && l_aux) {
+    float s = 0.f;
+    for (int e = 0; e < N; ++e) s += fp[e];
+    *l_aux = alpha * static_cast<float>(N) * s;
+  }
+}
+
+template <typename Tx>
+cudaError_t launch_router_t(const moe_config& c, const Tx* x, const float* w_r, const float* b_r,
+                            int32_t* idx, float* gate, float* psum, int32_t* pcnt,
+                            uint32_t* status, cudaStream_t s) {
+  const int nblk = (c.T + BM - 1) / BM;
+  const int N = c.n_experts;
+  dim3 grid(nblk), block(kThreads);
+#define MOE_ROUTER(NPW, WSN)                                                                  \
+  router_kernel<Tx, NPW, WSN><<<grid, block, 0, s>>>(x, w_r, b_r, c.T, c.d_model, N, c.top_k, \
+                                                     idx, gate, psum, pcnt, status)
+  if (N <= 8) MOE_ROUTER(8, 1);
+  else if (N <= 32) MOE_ROUTER(32, 1);
+  else if (N <= 64) MOE_ROUTER(32, 2);
+  else if (N <= 128) MOE_ROUTER(32, 4);
+  else MOE_ROUTER(32, 8);
+#undef MOE_ROUTER
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+moe_status launch_router(const moe_config& c, const void* x, const float* w_r, const float* b_r,
+                         int32_t* idx, float* gate, float* psum, int32_t* pcnt,
+                         const moe_stats* st, cudaStream_t s) {
+  if (c.T == 0) return MOE_OK;
+  uint32_t* status = st ? st->status : nullptr;
+  cudaError_t err;
+  if (c.dtype == MOE_BF16)
+    err = launch_router_t(c, static_cast<const __nv_bfloat16*>(x), w_r, b_r, idx, gate, psum, pcnt,
+                          status, s);
+  else
+    err = launch_router_t(c, static_cast<const float*>(x), w_r, b_r, idx, gate, psum, pcnt,
+                          status, s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  if (st && (st->count || st->f || st->P || st->l_aux)) {
+    const int nblk = (c.T + BM - 1) / BM;
+    route_stats_kernel<<<1, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k, c.alpha,
+                                         st->count, st->f, st->P, st->l_aux);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,321 @@
+"""Python binding of libmoe (include/moe.h) over ctypes.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels. Tensors are torch CUDA tensors (device memory and streams come from
+PyTorch); each function passes their device pointers and the current CUDA
+stream to the C entry point of the same name and raises MoEError when the
+status is not MOE_OK. There is no CPU path: without the built library or a
+CUDA device every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
+MOE_ERR_TIMEOUT, MOE_ERR_NONFINITE, MOE_ERR_WORKSPACE, MOE_ERR_INDEX = 4, 5, 6, 7
+MOE_F32, MOE_BF16 = 0, 1
+MOE_SWIGLU, MOE_GELU = 0, 1
+
+# Every symbol the header declares, in declaration order.
+EXPORTED = ["moe_workspace_size", "moe_capacity", "moe_route", "moe_dispatch",
+            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_status_string",
+            "moe_trace_events", "moe_ffn_uses_tensor_cores"]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+class MoEConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("activation", ctypes.c_int32),
+                ("has_bias", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
+                ("alpha", ctypes.c_float), ("add_residual", ctypes.c_int32)]
+
+
+class MoEStatsC(ctypes.Structure):
+    _fields_ = [("count", ctypes.c_void_p), ("kept", ctypes.c_void_p),
+                ("n_dropped", ctypes.c_void_p), ("f", ctypes.c_void_p), ("P", ctypes.c_void_p),
+                ("l_aux", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+
+
+class MoEExpertWeightsC(ctypes.Structure):
+    _fields_ = [("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("w1", ctypes.c_void_p), ("b1", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("b2", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (built in-tree); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmoe.so not found at {path}: build it with "
+                           "`python -m mixture_experts_layer_101_b300.build`")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    cfgp = ctypes.POINTER(MoEConfig)
+    statp = ctypes.POINTER(MoEStatsC)
+    wp = ctypes.POINTER(MoEExpertWeightsC)
+    lib.moe_workspace_size.argtypes = [cfgp]
+    lib.moe_workspace_size.restype = ctypes.c_size_t
+    lib.moe_capacity.argtypes = [cfgp]
+    lib.moe_capacity.restype = ctypes.c_int32
+    lib.moe_ffn_uses_tensor_cores.argtypes = [cfgp]
+    lib.moe_ffn_uses_tensor_cores.restype = ctypes.c_int32
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_route.argtypes = [cfgp, P, P, P, P, P, statp, P, P]
+    lib.moe_dispatch.argtypes = [cfgp, P, P, P, P, P, P, statp, P, P]
+    lib.moe_expert_ffn.argtypes = [cfgp, P, P, wp, P, statp, P, P]
+    lib.moe_combine.argtypes = [cfgp, P, P, P, P, P, P]
+    lib.moe_forward.argtypes = [cfgp, P, P, P, wp, P, statp, P, P]
+    lib.moe_trace_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
+    lib.moe_trace_events.restype = ctypes.c_int
+    for name in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().moe_status_string(int(code)).decode()
+
+
+moe_status_string = status_string
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+@dataclass
+class LayerConfig:
+    T: int
+    d_model: int
+    d_ff: int
+    n_experts: int
+    top_k: int
+    dtype: str = "bf16"
+    activation: str = "swiglu"
+    has_bias: bool = False
+    capacity_factor: float = math.inf
+    alpha: float = 0.01
+    add_residual: bool = False
+
+    @classmethod
+    def from_workload(cls, w, T: int | None = None) -> "LayerConfig":
+        return cls(T=w.T if T is None else T, d_model=w.d, d_ff=w.F, n_experts=w.N, top_k=w.K,
+                   dtype=w.dtype, activation=w.activation, has_bias=w.has_bias,
+                   capacity_factor=w.capacity_factor, alpha=w.alpha, add_residual=w.add_residual)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def c(self) -> MoEConfig:
+        return MoEConfig(self.T, self.d_model, self.d_ff, self.n_experts, self.top_k,
+                         MOE_BF16 if self.dtype == "bf16" else MOE_F32,
+                         MOE_SWIGLU if self.activation == "swiglu" else MOE_GELU,
+                         int(self.has_bias), float(self.capacity_factor), float(self.alpha),
+                         int(self.add_residual))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("libmoe takes CUDA tensors only (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError("libmoe takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(code: int, where: str):
+    if code != MOE_OK:
+        raise MoEError(code, where)
+
+
+class Stats:
+    """Device tensors for the layer statistics (count, kept, n_dropped, f, P,
+    l_aux, status)."""
+
+    def __init__(self, n_experts: int, device="cuda"):
+        i32, f32 = torch.int32, torch.float32
+        self.count = torch.zeros(n_experts, dtype=i32, device=device)
+        self.kept = torch.zeros(n_experts, dtype=i32, device=device)
+        self.n_dropped = torch.zeros(1, dtype=i32, device=device)
+        self.f = torch.zeros(n_experts, dtype=f32, device=device)
+        self.P = torch.zeros(n_experts, dtype=f32, device=device)
+        self.l_aux = torch.zeros(1, dtype=f32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def c(self) -> MoEStatsC:
+        return MoEStatsC(*(_ptr(t) for t in (self.count, self.kept, self.n_dropped, self.f,
+                                             self.P, self.l_aux, self.status)))
+
+    def status_bits(self) -> int:
+        return int(self.status.item()) & 0xFFFFFFFF
+
+    def to_host(self) -> dict:
+        return {"count": self.count.cpu().numpy(), "kept": self.kept.cpu().numpy(),
+                "n_dropped": int(self.n_dropped.item()), "f": self.f.cpu().numpy(),
+                "P": self.P.cpu().numpy(), "l_aux": float(self.l_aux.item()),
+                "status": self.status_bits()}
+
+
+def weights_c(weights: dict) -> MoEExpertWeightsC:
+    names = ("w_gate", "w_up", "w_down", "w1", "b1", "w2", "b2")
+    return MoEExpertWeightsC(*(_ptr(weights.get(n)) for n in names))
+
+
+def workspace_size(cfg: LayerConfig) -> int:
+    return int(load_library().moe_workspace_size(ctypes.byref(cfg.c())))
+
+
+moe_workspace_size = workspace_size
+
+
+def capacity(cfg: LayerConfig) -> int:
+    return int(load_library().moe_capacity(ctypes.byref(cfg.c())))
+
+
+moe_capacity = capacity
+
+
+def ffn_uses_tensor_cores(cfg: LayerConfig) -> bool:
+    return load_library().moe_ffn_uses_tensor_cores(ctypes.byref(cfg.c())) == 1
+
+
+moe_ffn_uses_tensor_cores = ffn_uses_tensor_cores
+
+
+def a_max(cfg: LayerConfig) -> int:
+    C = capacity(cfg)
+    return min(cfg.T * cfg.top_k, cfg.n_experts * C)
+
+
+def alloc_workspace(cfg: LayerConfig, device="cuda") -> torch.Tensor:
+    """A byte tensor of moe_workspace_size(cfg) bytes (torch allocations are
+    at least 256-byte aligned)."""
+    n = workspace_size(cfg)
+    if n == 0:
+        raise MoEError(MOE_ERR_INVALID, "moe_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+# --------------------------------------------------------------------------
+# the C entry points, one by one
+# --------------------------------------------------------------------------
+def moe_route(cfg: LayerConfig, x, w_r, b_r, idx, gate, stats: Stats | None, ws, stream=None):
+    lib = load_library()
+    st = stats.c() if stats is not None else None
+    code = lib.moe_route(ctypes.byref(cfg.c()), _ptr(x), _ptr(w_r), _ptr(b_r), _ptr(idx),
+                         _ptr(gate), ctypes.byref(st) if st is not None else None, _ptr(ws),
+                         _stream(stream))
+    _check(code, "moe_route")
+
+
+def moe_dispatch(cfg: LayerConfig, x, idx, offsets, slot_of, token_of_slot, x_perm,
+                 stats: Stats | None, ws, stream=None):
+    lib = load_library()
+    st = stats.c() if stats is not None else None
+    code = lib.moe_dispatch(ctypes.byref(cfg.c()), _ptr(x), _ptr(idx), _ptr(offsets),
+                            _ptr(slot_of), _ptr(token_of_slot), _ptr(x_perm),
+                            ctypes.byref(st) if st is not None else None, _ptr(ws),
+                            _stream(stream))
+    _check(code, "moe_dispatch")
+
+
+def moe_expert_ffn(cfg: LayerConfig, x_perm, offsets, weights: dict, o, stats: Stats | None, ws,
+                   stream=None):
+    lib = load_library()
+    st = stats.c() if stats is not None else None
+    wc = weights_c(weights)
+    code = lib.moe_expert_ffn(ctypes.byref(cfg.c()), _ptr(x_perm), _ptr(offsets),
+                              ctypes.byref(wc), _ptr(o),
+                              ctypes.byref(st) if st is not None else None, _ptr(ws),
+                              _stream(stream))
+    _check(code, "moe_expert_ffn")
+
+
+def moe_combine(cfg: LayerConfig, o, slot_of, gate, x, y, stream=None):
+    lib = load_library()
+    code = lib.moe_combine(ctypes.byref(cfg.c()), _ptr(o), _ptr(slot_of), _ptr(gate), _ptr(x),
+                           _ptr(y), _stream(stream))
+    _check(code, "moe_combine")
+
+
+def moe_forward(cfg: LayerConfig, x, w_r, b_r, weights: dict, y, stats: Stats | None, ws,
+                stream=None):
+    lib = load_library()
+    st = stats.c() if stats is not None else None
+    wc = weights_c(weights)
+    code = lib.moe_forward(ctypes.byref(cfg.c()), _ptr(x), _ptr(w_r), _ptr(b_r),
+                           ctypes.byref(wc), _ptr(y), ctypes.byref(st) if st is not None else None,
+                           _ptr(ws), _stream(stream))
+    _check(code, "moe_forward")
+
+
+def moe_trace_events(events):
+    """Register torch.cuda.Event objects (at most 6, enable_timing=True) that
+    moe_forward records at its stage boundaries on this host thread; pass
+    [] to clear. Keep the events alive while registered."""
+    lib = load_library()
+    arr = (ctypes.c_void_p * max(len(events), 1))(*[ctypes.c_void_p(e.cuda_event)
+                                                      for e in events])
+    _check(lib.moe_trace_events(arr if events else None, len(events)), "moe_trace_events")
+
+
+TRACE_STAGES = ["router", "dispatch", "ffn_gate_up", "ffn_down", "combine"]
+
+
+class MoELayer:
+    """A sparse-MoE FFN layer with its weights, workspace and statistics held
+    on one CUDA device; forward() runs moe_forward."""
+
+    def __init__(self, cfg: LayerConfig, w_r, b_r, weights: dict, device="cuda"):
+        self.cfg = cfg
+        self.w_r = w_r
+        self.b_r = b_r
+        self.weights = weights
+        self.ws = alloc_workspace(cfg, device)
+        self.stats = Stats(cfg.n_experts, device)
+        self.y = torch.empty((cfg.T, cfg.d_model), dtype=cfg.torch_dtype, device=device)
+
+    def forward(self, x, stream=None):
+        moe_forward(self.cfg, x, self.w_r, self.b_r, self.weights, self.y, self.stats, self.ws,
+                    stream)
+        return self.y
+
+    def forward_host(self, x_host, y_host, x_dev, stream=None):
+        """End-to-end call on host buffers: copy x (pinned host) in, run the
+        layer, copy y and L_aux back; returns L_aux (a host float tensor)."""
+        x_dev.copy_(x_host, non_blocking=True)
+        self.forward(x_dev, stream)
+        y_host.copy_(self.y, non_blocking=True)
+        return self.stats.l_aux.to("cpu", non_blocking=True)

@@ -1,0 +1,132 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C
+ABI (stage by stage, or whole), and compare with the float64 oracle.
+
+Comparison rules:
+  * routing: bit-exact expert indices except on near-tie tokens (some adjacent
+    gap among the K+1 largest float64 logits below 1e-5); a near-tie token's
+    GPU choice is accepted when each chosen expert's float64 logit lies within
+    1e-5 of the oracle's choice at the same rank; everything downstream is then
+    compared against the oracle re-run on the GPU's routing;
+  * counts, kept, offsets, slots, token order and the drop set: bit-exact;
+  * gates: |err| <= 1e-5; P and L_aux: relative error <= 1e-5;
+  * y: max |err| <= 1e-4 * rms(y) for fp32 layers, <= 2e-2 * rms(y) for bf16.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import mixture_experts_layer_101_b300 as moe
+import moe_inputs
+from oracle import moe_oracle as O
+
+NEAR_TIE_EPS = 1e-5
+GATE_TOL = 1e-5
+STAT_RTOL = 1e-5
+
+
+def y_tolerance(dtype: str) -> float:
+    return 1e-4 if dtype == "f32" else 2e-2
+
+
+def device_inputs(w: moe_inputs.MoEWorkload):
+    """Inputs on cuda:0; x and the router drawn on the CPU, experts on the GPU."""
+    x = moe_inputs.make_x(w)
+    w_r, b_r = moe_inputs.make_router(w)
+    experts = moe_inputs.make_experts(w, "cuda")
+    return {"x": x.cuda(), "w_r": w_r.cuda(), "b_r": None if b_r is None else b_r.cuda(),
+            "experts": experts}
+
+
+def expert_reader(experts: dict):
+    """expert_of(e) for the oracle: copies expert e's weights to the host."""
+    return lambda e: {k: v[e].cpu() for k, v in experts.items()}
+
+
+def run_stages(cfg: moe.LayerConfig, inp: dict) -> dict:
+    """route -> dispatch -> expert_ffn -> combine through the C ABI."""
+    dev = "cuda"
+    T, K, N, d = cfg.T, cfg.top_k, cfg.n_experts, cfg.d_model
+    A = moe.a_max(cfg)
+    ws = moe.alloc_workspace(cfg)
+    st = moe.Stats(N)
+    idx = torch.full((T, K), -7, dtype=torch.int32, device=dev)
+    gate = torch.zeros((T, K), dtype=torch.float32, device=dev)
+    moe.moe_route(cfg, inp["x"], inp["w_r"], inp["b_r"], idx, gate, st, ws)
+    offsets = torch.zeros(N + 1, dtype=torch.int32, device=dev)
+    slot_of = torch.full((T, K), -7, dtype=torch.int32, device=dev)
+    tos = torch.full((max(A, 1),), -7, dtype=torch.int32, device=dev)
+    x_perm = torch.zeros((max(A, 1), d), dtype=cfg.torch_dtype, device=dev)
+    moe.moe_dispatch(cfg, inp["x"], idx, offsets, slot_of, tos, x_perm, st, ws)
+    o = torch.zeros((max(A, 1), d), dtype=torch.float32, device=dev)
+    moe.moe_expert_ffn(cfg, x_perm, offsets, inp["experts"], o, st, ws)
+    y = torch.zeros((T, d), dtype=cfg.torch_dtype, device=dev)
+    moe.moe_combine(cfg, o, slot_of, gate, inp["x"], y)
+    torch.cuda.synchronize()
+    out = {"idx": idx, "gate": gate, "offsets": offsets, "slot_of": slot_of,
+           "token_of_slot": tos, "x_perm": x_perm, "o": o, "y": y}
+    out = {k: v.cpu() for k, v in out.items()}
+    out["stats"] = st.to_host()
+    return out
+
+
+def run_forward(cfg: moe.LayerConfig, inp: dict):
+    layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
+    y = layer.forward(inp["x"]).clone()
+    torch.cuda.synchronize()
+    return y.cpu(), layer.stats.to_host()
+
+
+def check_routing(l64: np.ndarray, idx_gpu: np.ndarray, K: int):
+    """Returns (near-tie token count, tokens whose routing differs)."""
+    idx_o = O.topk_experts(l64, K)
+    near = O.near_tie_tokens(l64, K, NEAR_TIE_EPS)
+    diff = np.any(idx_gpu != idx_o, axis=1)
+    bad = diff & ~near
+    assert not bad.any(), f"routing differs on {bad.sum()} tokens without a near-tie"
+    for t in np.nonzero(diff)[0]:
+        assert len(set(idx_gpu[t].tolist())) == K
+        assert np.all(np.abs(l64[t, idx_gpu[t]] - l64[t, idx_o[t]]) < NEAR_TIE_EPS)
+    return int(near.sum()), int(diff.sum())
+
+
+def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None, check_o=True):
+    """Compare a stage-wise GPU run against the oracle. tokens: the tokens
+    whose y is checked (None = all); routing, statistics and dispatch always
+    cover every token. Returns a summary dict."""
+    K, N = cfg.top_k, cfg.n_experts
+    x, w_r, b_r = inp["x"].cpu(), inp["w_r"].cpu(), None if inp["b_r"] is None else inp["b_r"].cpu()
+    l64 = O.router_logits(x, w_r, b_r)
+    idx_gpu = gpu["idx"].numpy().astype(np.int64)
+    n_near, n_diff = check_routing(l64, idx_gpu, K)
+    ref = O.moe_forward(x, w_r, b_r, expert_reader(inp["experts"]), K=K,
+                        activation=cfg.activation, capacity_factor=cfg.capacity_factor,
+                        alpha=cfg.alpha, add_residual=cfg.add_residual, tokens=tokens,
+                        idx_override=idx_gpu)
+    # gates and statistics
+    assert np.max(np.abs(gpu["gate"].numpy() - ref["gate"]), initial=0) <= GATE_TOL
+    st = gpu["stats"]
+    assert np.array_equal(st["count"], ref["count"])
+    assert np.allclose(st["P"], ref["P"], rtol=STAT_RTOL, atol=1e-7)
+    assert np.allclose(st["f"], ref["f"], rtol=1e-6, atol=0)
+    assert abs(st["l_aux"] - ref["l_aux"]) <= STAT_RTOL * abs(ref["l_aux"]) + 1e-9
+    assert st["status"] == 0
+    # dispatch: bit-exact
+    assert np.array_equal(st["kept"], ref["kept"])
+    assert st["n_dropped"] == ref["n_dropped"]
+    assert np.array_equal(gpu["offsets"].numpy(), ref["offsets"])
+    assert np.array_equal(gpu["slot_of"].numpy(), ref["slot_of"])
+    A = int(ref["offsets"][-1])
+    assert np.array_equal(gpu["token_of_slot"].numpy()[:A], ref["token_of_slot"])
+    if A > 0:
+        tos = torch.from_numpy(ref["token_of_slot"])
+        assert torch.equal(gpu["x_perm"][:A], inp["x"].cpu()[tos])
+    # outputs
+    tok = ref["tokens"]
+    y_gpu = gpu["y"].double().numpy()[tok]
+    y_ref = ref["y"]
+    rms = float(np.sqrt(np.mean(y_ref ** 2))) if y_ref.size else 0.0
+    err = float(np.max(np.abs(y_gpu - y_ref))) if y_ref.size else 0.0
+    assert err <= y_tolerance(cfg.dtype) * rms + 1e-30, (err, rms)
+    return {"near_ties": n_near, "routing_diff": n_diff, "A": A, "y_err_over_rms":
+            err / rms if rms > 0 else 0.0, "n_dropped": ref["n_dropped"]}

@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the float64
+oracle on the same seeded inputs.
+
+Small shapes (every token checked) span several tiles with ragged tails and
+cover both expert-FFN paths (tcgen05 tensor cores and CUDA cores); the five
+named workloads run at full size with routing, statistics and dispatch
+checked on every token and y on a sample of tokens.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+from moe_inputs import MoEWorkload
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import mixture_experts_layer_101_b300 as moe
+    import moe_testlib as L
+
+
+def wl(name="case", **kw):
+    base = dict(T=100, d=256, F=128, N=4, K=2)
+    base.update(kw)
+    return MoEWorkload(name, **base)
+
+
+SMALL = {
+    # tensor-core path: d % 256 == 0, F % 128 == 0, bf16 SwiGLU
+    "tc_ragged": wl(T=300, d=256, F=256, N=3, K=2),
+    "tc_multi_tile": wl(T=700, d=512, F=384, N=5, K=2),
+    "tc_top1_capacity": wl(T=1000, d=256, F=128, N=8, K=1, capacity_factor=1.25,
+                           add_residual=True, router_bias="skew"),
+    "tc_k_eq_n": wl(T=64, d=256, F=128, N=4, K=4),
+    "tc_single_expert": wl(T=129, d=256, F=256, N=1, K=1),
+    "tc_top8_of_64": wl(T=257, d=512, F=256, N=64, K=8),
+    "tc_one_token": wl(T=1, d=256, F=128, N=8, K=2),
+    "tc_k3_odd_n": wl(T=200, d=256, F=128, N=7, K=3, capacity_factor=1.0),
+    # CUDA-core path: fp32, GELU, or shapes the tensor-core kernel does not tile
+    "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
+    "simt_gelu_nobias": wl(T=90, d=64, F=96, N=4, K=2, dtype="f32", activation="gelu",
+                           init="uniform"),
+    "simt_bf16_odd_d": wl(T=150, d=72, F=100, N=6, K=2),
+    "simt_fp32_swiglu": wl(T=77, d=36, F=52, N=5, K=3, dtype="f32", init="uniform"),
+    "simt_gelu_capacity": wl(T=128, d=64, F=128, N=4, K=2, dtype="f32", activation="gelu",
+                             has_bias=True, init="uniform", router_bias="uniform",
+                             capacity_factor=0.5, add_residual=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_layers_stagewise(name):
+    w = SMALL[name]
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    gpu = L.run_stages(cfg, inp)
+    summary = L.check_layer(cfg, inp, gpu)
+    assert summary["routing_diff"] == 0 or summary["near_ties"] > 0
+
+
+@pytest.mark.parametrize("name", ["tc_ragged", "tiny_fp32", "tc_top1_capacity"])
+def test_forward_equals_stages_and_is_deterministic(name):
+    w = SMALL[name]
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    gpu = L.run_stages(cfg, inp)
+    y1, st1 = L.run_forward(cfg, inp)
+    y2, st2 = L.run_forward(cfg, inp)
+    assert torch.equal(y1, y2) and torch.equal(y1, gpu["y"])
+    for k in ("count", "kept", "f", "P"):
+        assert np.array_equal(st1[k], st2[k]) and np.array_equal(st1[k], gpu["stats"][k])
+    assert st1["l_aux"] == st2["l_aux"] == gpu["stats"]["l_aux"]
+
+
+def test_tensor_core_path_is_selected():
+    assert moe.ffn_uses_tensor_cores(moe.LayerConfig.from_workload(SMALL["tc_ragged"]))
+    assert not moe.ffn_uses_tensor_cores(moe.LayerConfig.from_workload(SMALL["tiny_fp32"]))
+    for name in ("mixtral_prefill", "mixtral_decode", "deepseek_fine", "switch_skewed"):
+        assert moe.ffn_uses_tensor_cores(
+            moe.LayerConfig.from_workload(moe_inputs.WORKLOADS[name]))
+
+
+def test_zero_capacity_drops_everything():
+    for residual in (False, True):
+        w = wl(T=96, d=256, F=128, N=4, K=2, capacity_factor=0.01, add_residual=residual)
+        cfg = moe.LayerConfig.from_workload(w)
+        assert moe.capacity(cfg) == 0
+        inp = L.device_inputs(w)
+        gpu = L.run_stages(cfg, inp)
+        assert gpu["stats"]["n_dropped"] == 96 * 2
+        assert (gpu["slot_of"] == -1).all()
+        expect = inp["x"].cpu() if residual else torch.zeros_like(inp["x"].cpu())
+        assert torch.equal(gpu["y"], expect)
+
+
+def test_empty_batch_is_a_no_op():
+    """T = 0 is accepted and touches nothing (buffers are placeholders)."""
+    w1 = wl(T=1, d=256, F=128, N=4, K=2)
+    cfg = moe.LayerConfig.from_workload(wl(T=0, d=256, F=128, N=4, K=2))
+    inp = L.device_inputs(w1)
+    y = torch.full((1, 256), 3.0, dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(cfg)
+    st = moe.Stats(4)
+    moe.moe_forward(cfg, inp["x"], inp["w_r"], None, inp["experts"], y, st, ws)
+    torch.cuda.synchronize()
+    assert st.status_bits() == 0
+    assert (y == 3.0).all()
+    assert int(st.n_dropped.item()) == 0 and int(st.kept.sum()) == 0
+
+
+def test_nonfinite_logit_sets_status():
+    w = wl(T=64, d=256, F=128, N=4, K=2)
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    inp["x"][5, 7] = float("nan")
+    layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
+    layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert layer.stats.status_bits() & (1 << moe.moe.MOE_ERR_NONFINITE)
+    # routing indices stay in range whatever the logits
+    idx = torch.empty((64, 2), dtype=torch.int32, device="cuda")
+    gate = torch.empty((64, 2), dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, inp["x"], inp["w_r"], None, idx, gate, None, layer.ws)
+    torch.cuda.synchronize()
+    assert int(idx.min()) >= 0 and int(idx.max()) < 4
+
+
+def test_bad_expert_index_sets_status_and_drops():
+    w = wl(T=40, d=256, F=128, N=4, K=2)
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    idx = torch.randint(0, 4, (40, 2), dtype=torch.int32, device="cuda")
+    idx[3, 1] = 9
+    idx[7, 0] = -2
+    A = moe.a_max(cfg)
+    offsets = torch.zeros(5, dtype=torch.int32, device="cuda")
+    slot_of = torch.zeros((40, 2), dtype=torch.int32, device="cuda")
+    tos = torch.zeros(A, dtype=torch.int32, device="cuda")
+    xp = torch.zeros((A, 256), dtype=torch.bfloat16, device="cuda")
+    st = moe.Stats(4)
+    moe.moe_dispatch(cfg, inp["x"], idx, offsets, slot_of, tos, xp, st, moe.alloc_workspace(cfg))
+    torch.cuda.synchronize()
+    assert st.status_bits() & (1 << moe.moe.MOE_ERR_INDEX)
+    assert int(slot_of[3, 1]) == -1 and int(slot_of[7, 0]) == -1
+    assert int(offsets[-1]) == 78
+
+
+def test_host_errors_launch_nothing():
+    w = wl(T=64, d=256, F=128, N=4, K=2)
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    y = torch.empty_like(inp["x"])
+    ws = moe.alloc_workspace(cfg)
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_forward(cfg, inp["x"], inp["w_r"], None, inp["experts"], y, None, ws[1:])
+    assert e.value.code == moe.moe.MOE_ERR_WORKSPACE
+    bad = moe.LayerConfig.from_workload(w)
+    bad.top_k = 5
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_forward(bad, inp["x"], inp["w_r"], None, inp["experts"], y, None, ws)
+    assert e.value.code == moe.moe.MOE_ERR_INVALID
+    missing = dict(inp["experts"])
+    missing.pop("w_up")
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_forward(cfg, inp["x"], inp["w_r"], None, missing, y, None, ws)
+    assert e.value.code == moe.moe.MOE_ERR_INVALID
+    with pytest.raises(ValueError):
+        moe.moe_forward(cfg, inp["x"].cpu(), inp["w_r"], None, inp["experts"], y, None, ws)
+
+
+# ------------------------------------------------ the named workloads ----
+FULL_SAMPLE = {"mixtral_prefill": 24, "mixtral_decode": 16, "deepseek_fine": 8,
+               "switch_skewed": 48}
+
+
+@pytest.mark.parametrize("name", ["mixtral_decode", "switch_skewed", "mixtral_prefill",
+                                  "deepseek_fine"])
+def test_full_size_workload(name):
+    w = moe_inputs.WORKLOADS[name]
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    gpu = L.run_stages(cfg, inp)
+    rng = np.random.default_rng(12345)
+    n = min(FULL_SAMPLE[name], w.T)
+    tokens = np.sort(rng.choice(w.T, size=n, replace=False))
+    if name == "switch_skewed":  # include dropped tokens: their y must equal x
+        dropped = np.nonzero((gpu["slot_of"].numpy() < 0).all(axis=1))[0]
+        tokens = np.union1d(tokens, dropped[:8])
+    summary = L.check_layer(cfg, inp, gpu, tokens=tokens)
+    y_fwd, _ = L.run_forward(cfg, inp)
+    assert torch.equal(y_fwd, gpu["y"])
+    if name == "switch_skewed":
+        assert moe.capacity(cfg) == 640
+        assert summary["n_dropped"] > 0
+    del inp
+    torch.cuda.empty_cache()
