@@ -99,13 +99,59 @@ def sum_over_ranks(value: float, world: int) -> float:
 # ----------------------------------------------------------------------------
 # clocks during the timed region (read-only NVML queries)
 # ----------------------------------------------------------------------------
+class _NvmlReader:
+    """Read-only NVML queries through ctypes (clock, max clock, clock-event
+    reasons) for the GPU torch is using."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        ok = False
+        try:
+            uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            ok = self.lib.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(),
+                                                    ctypes.byref(self.handle)) == 0
+        except Exception:
+            ok = False
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.handle)) != 0:
+            raise RuntimeError("no NVML device handle")
+        try:
+            self._reasons_fn = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_mhz(self):
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, self.ct.byref(v))
+        return int(v.value)
+
+    def sm_max_mhz(self):
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.NVML_CLOCK_SM, self.ct.byref(v))
+        return int(v.value)
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        self._reasons_fn(self.handle, self.ct.byref(v))
+        return int(v.value)
+
+
 class ClockSampler:
+    """Samples the SM clock and the clock-event reasons every few ms while the
+    timed region runs (read-only; changes no GPU setting)."""
+
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks", 0x4: "sw_power_cap",
                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x100: "display_clock"}
 
-    def __init__(self, period_s=0.02):
+    def __init__(self, period_s=0.005):
         self.period = period_s
         self.samples = []
         self.reason_bits = 0
@@ -114,34 +160,17 @@ class ClockSampler:
         self._thread = None
         self.error = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nvml = pynvml
-            self.handle = self._handle()
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM)
+            self.nvml = _NvmlReader()
+            self.max_mhz = self.nvml.sm_max_mhz()
         except Exception as e:  # no NVML: report nothing rather than guess
             self.nvml = None
             self.error = f"nvml unavailable: {e}"
 
-    def _handle(self):
-        p = self.nvml
-        try:
-            uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
-            return p.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode())
-        except Exception:
-            return p.nvmlDeviceGetHandleByIndex(0)
-
     def _run(self):
-        p = self.nvml
         while not self._stop.is_set():
             try:
-                mhz = p.nvmlDeviceGetClockInfo(self.handle, p.NVML_CLOCK_SM)
-                try:
-                    bits = p.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
-                except Exception:
-                    bits = p.nvmlDeviceGetCurrentClocksThrottleReasons(self.handle)
-                self.samples.append(mhz)
-                self.reason_bits |= int(bits)
+                self.samples.append(self.nvml.sm_mhz())
+                self.reason_bits |= self.nvml.reasons()
             except Exception as e:
                 self.error = str(e)
                 return
@@ -225,7 +254,14 @@ def roofline_entry(flops, nbytes, seconds, peaks, sustained=False):
 # ----------------------------------------------------------------------------
 # CPU oracle timing (baseline and reference arm)
 # ----------------------------------------------------------------------------
+F64_HOST_LIMIT = 16 << 30
+
+
 def host_inputs(w, experts_dev=None):
+    """The workload's inputs on the host. Expert weights are handed to the
+    oracle already in float64 when that fits in F64_HOST_LIMIT bytes (the
+    oracle's own promotion is then a no-op); otherwise the oracle promotes
+    each expert it needs, inside the timed call."""
     x = moe_inputs.make_x(w)
     w_r, b_r = moe_inputs.make_router(w)
     if experts_dev is not None:
@@ -234,6 +270,8 @@ def host_inputs(w, experts_dev=None):
         experts = {k: v.cpu() for k, v in moe_inputs.make_experts(w, "cuda").items()}
     else:
         experts = moe_inputs.make_experts(w, "cpu")
+    if sum(v.numel() for v in experts.values()) * 8 <= F64_HOST_LIMIT:
+        experts = {k: v.double().numpy() for k, v in experts.items()}
     return x, w_r, b_r, experts
 
 
@@ -263,10 +301,12 @@ def cpu_baseline(w, experts_dev, budget_s=15.0):
     while n < w.T and t < budget_s / 4:
         n = min(w.T, n * 4)
         t = time_oracle(w, x, w_r, b_r, experts, n)
+    pre = isinstance(next(iter(experts.values())), __import__("numpy").ndarray)
     return {"value": round(n / t, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
             "sample": f"float64 oracle: routing/statistics/dispatch of all {w.T} tokens, "
                       f"experts and combine of the first {n} tokens; {t:.2f} s; "
-                      f"value = {n} tokens / that time"}
+                      f"value = {n} tokens / that time; expert weights "
+                      + ("given in float64" if pre else "promoted by the oracle per call")}
 
 
 def run_reference(args, world, rank):
@@ -331,23 +371,22 @@ def run_ours(args, world, rank):
     torch.cuda.synchronize()
     layer.stats.status.zero_()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)]
-              for _ in range(args.steps)]
+    events = [moe.TraceEvents(nst) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler() as clocks:
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
-            moe.moe_trace_events(events[i])
+            moe.moe_trace_events(events[i].handles())
             layer.forward(x)
         moe.moe_trace_events([])
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     barrier(world)
 
-    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
-    stage_ms = {name: [ev[j].elapsed_time(ev[j + 1]) for ev in events]
+    step_ms = [ev.elapsed_ms(0, nst - 1) for ev in events]
+    stage_ms = {name: [ev.elapsed_ms(j, j + 1) for ev in events]
                 for j, name in enumerate(moe.TRACE_STAGES)}
     dev_s = sum(step_ms) / 1e3
     max_s = max_over_ranks(dev_s, world)
@@ -422,7 +461,7 @@ def run_ours(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="mixtral_prefill", choices=sorted(moe_inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -282,13 +282,48 @@ def moe_forward(cfg: LayerConfig, x, w_r, b_r, weights: dict, y, stats: Stats | 
 
 
 def moe_trace_events(events):
-    """Register torch.cuda.Event objects (at most 6, enable_timing=True) that
-    moe_forward records at its stage boundaries on this host thread; pass
-    [] to clear. Keep the events alive while registered."""
+    """Register up to 6 raw CUDA event handles (ints, e.g. TraceEvents.handles)
+    that moe_forward records at its stage boundaries on this host thread;
+    pass [] to clear. The caller keeps the events alive while registered."""
     lib = load_library()
-    arr = (ctypes.c_void_p * max(len(events), 1))(*[ctypes.c_void_p(e.cuda_event)
-                                                      for e in events])
+    arr = (ctypes.c_void_p * max(len(events), 1))(*[ctypes.c_void_p(int(e)) for e in events])
     _check(lib.moe_trace_events(arr if events else None, len(events)), "moe_trace_events")
+
+
+class TraceEvents:
+    """A set of raw CUDA events for moe_trace_events, created and timed with
+    the CUDA runtime bindings (torch.cuda.Event cannot time events that it
+    did not record itself)."""
+
+    def __init__(self, n: int = 6):
+        from cuda.bindings import runtime as rt
+        self._rt = rt
+        self.events = []
+        for _ in range(n):
+            err, ev = rt.cudaEventCreate()
+            if err != rt.cudaError_t.cudaSuccess:
+                raise RuntimeError(f"cudaEventCreate failed: {err}")
+            self.events.append(ev)
+
+    def handles(self):
+        return [int(e) for e in self.events]
+
+    def elapsed_ms(self, i: int, j: int) -> float:
+        err, ms = self._rt.cudaEventElapsedTime(self.events[i], self.events[j])
+        if err != self._rt.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"cudaEventElapsedTime failed: {err}")
+        return float(ms)
+
+    def close(self):
+        for e in self.events:
+            self._rt.cudaEventDestroy(e)
+        self.events = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 TRACE_STAGES = ["router", "dispatch", "ffn_gate_up", "ffn_down", "combine"]
