@@ -152,6 +152,30 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r,
                      const float* b_r, int32_t* idx, float* gate,
                      moe_stats* stats, void* ws, moe_stream_t stream);
 
+/* moe_route for callers that cannot allocate device memory (the pages have
+ * no counterpart: this is an interface variant, not a different method).
+ * A serving process whose device memory is all owned by its own pool, or a
+ * plug-in interface that passes no workspace, can call this instead of
+ * moe_route: same kernels, same results, but the per-block partial sums of
+ * the statistics live in a fixed array inside the library (1 MiB, held on
+ * every GPU that loads the library until the process exits) instead of a
+ * caller workspace. Nothing is allocated: no cudaMalloc, no cudaFree.
+ *   Limit: ceil(T / 32) * N <= 131072 (e.g. T <= 16384 with N = 256,
+ *   T <= 524288 with N = 8); beyond it returns MOE_ERR_WORKSPACE before
+ *   launching anything.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture on that device.
+ *   Sharing: all calls share the array and it keeps the last call's
+ *   contents; each call rewrites every element it reads, so nothing needs
+ *   clearing, but calls whose kernels overlap on the GPU (other streams or
+ *   host threads) race on it: serialise them.
+ * Arguments, outputs and errors are those of moe_route, without ws. */
+moe_status moe_route_no_workspace(const moe_config* cfg, const void* x,
+                                  const float* w_r, const float* b_r,
+                                  int32_t* idx, float* gate, moe_stats* stats,
+                                  moe_stream_t stream);
+
 /* Capacity-limited dispatch. Assignments are visited rank-major (k = 0..K-1,
  * then t = 0..T-1); an assignment (t, k) to expert e is kept iff fewer than C
  * earlier assignments went to e. Kept assignments of expert e occupy the

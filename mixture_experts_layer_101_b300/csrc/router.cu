@@ -19,6 +19,8 @@
 
 #include <float.h>
 
+#include <mutex>
+
 namespace moe {
 namespace {
 
@@ -281,3 +283,79 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Router without a caller workspace.
+//
+// Some callers cannot call cudaMalloc or hand the library a workspace: a
+// serving process whose device memory is all owned by its own pool and that
+// forbids any other allocation after start-up, or a plug-in interface whose
+// signature has no workspace argument. For them moe_route_no_workspace runs
+// the same router and statistics kernels as moe_route, with the per-block
+// partial sums held in the fixed array below instead of the workspace. The
+// array lives in every GPU that loads this library, until the process exits.
+//
+// Limit: ceil(T / 32) * N <= kRouteScratchElems (131072 = 1 MiB of scratch:
+// one fp32 and one int32 per (token block, expert)); larger requests return
+// MOE_ERR_WORKSPACE before anything is launched.
+//
+// Sharing: every call uses the same array. The router kernel writes every
+// partial it later reads, so nothing needs clearing between calls, but calls
+// whose kernels overlap on the GPU (different streams, or different host
+// threads) race on the array; serialise them.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr size_t kRouteScratchElems = 131072;
+static __device__ __align__(256) unsigned char g_route_scratch[kRouteScratchElems * 8];
+
+// Device address of g_route_scratch on each device, looked up once per
+// device with that device current (in host code the symbol's name is only a
+// host-side stand-in, never a device address).
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+moe_status route_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_route_no_workspace(const moe_config* cfg, const void* x,
+                                             const float* w_r, const float* b_r, int32_t* idx,
+                                             float* gate, moe_stats* stats,
+                                             moe_stream_t stream) {
+  using namespace moe;
+  try {
+    moe_status why = MOE_OK;
+    if (!config_valid(cfg, &why)) return why;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!x || !w_r || !idx || !gate) return MOE_ERR_INVALID;
+    if (!a16(x) || !a16(w_r) || !a16(idx) || !a16(gate) || (b_r && !a16(b_r)))
+      return MOE_ERR_INVALID;
+    const size_t nblk = (static_cast<size_t>(cfg->T) + BM - 1) / BM;
+    if (nblk * static_cast<size_t>(cfg->n_experts) > kRouteScratchElems) return MOE_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if (moe_status s = route_scratch_address(&scratch)) return s;
+    float* psum = static_cast<float*>(scratch);
+    int32_t* pcnt = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(scratch) +
+                                               kRouteScratchElems * sizeof(float));
+    return launch_router(*cfg, x, w_r, b_r, idx, gate, psum, pcnt, stats,
+                         static_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return MOE_ERR_CUDA;
+  }
+}

@@ -25,7 +25,8 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_SWIGLU, MOE_GELU = 0, 1
 
 # Every symbol the header declares, in declaration order.
-EXPORTED = ["moe_workspace_size", "moe_capacity", "moe_route", "moe_dispatch",
+EXPORTED = ["moe_workspace_size", "moe_capacity", "moe_route", "moe_route_no_workspace",
+            "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_status_string",
             "moe_trace_events", "moe_ffn_uses_tensor_cores"]
 
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_route.argtypes = [cfgp, P, P, P, P, P, statp, P, P]
+    lib.moe_route_no_workspace.argtypes = [cfgp, P, P, P, P, P, statp, P]
+    lib.moe_route_no_workspace.restype = ctypes.c_int
     lib.moe_dispatch.argtypes = [cfgp, P, P, P, P, P, P, statp, P, P]
     lib.moe_expert_ffn.argtypes = [cfgp, P, P, wp, P, statp, P, P]
     lib.moe_combine.argtypes = [cfgp, P, P, P, P, P, P]
@@ -238,6 +241,22 @@ def moe_route(cfg: LayerConfig, x, w_r, b_r, idx, gate, stats: Stats | None, ws,
                          _ptr(gate), ctypes.byref(st) if st is not None else None, _ptr(ws),
                          _stream(stream))
     _check(code, "moe_route")
+
+
+def moe_route_no_workspace(cfg: LayerConfig, x, w_r, b_r, idx, gate, stats: Stats | None,
+                           stream=None):
+    """moe_route without a workspace: for callers that cannot allocate device
+    memory. The library keeps the statistics' partial sums in a fixed 1 MiB
+    array (ceil(T/32) * N <= 131072); calls share it, so calls that overlap on
+    the GPU must not be issued. The first call on a device does a one-time
+    set-up; make it before any stream capture."""
+    lib = load_library()
+    st = stats.c() if stats is not None else None
+    code = lib.moe_route_no_workspace(ctypes.byref(cfg.c()), _ptr(x), _ptr(w_r), _ptr(b_r),
+                                      _ptr(idx), _ptr(gate),
+                                      ctypes.byref(st) if st is not None else None,
+                                      _stream(stream))
+    _check(code, "moe_route_no_workspace")
 
 
 def moe_dispatch(cfg: LayerConfig, x, idx, offsets, slot_of, token_of_slot, x_perm,
