@@ -327,6 +327,304 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 }
 
+// ---- CTA-pair variant (cta_group::2) -------------------------------------------
+// Two CTAs of a cluster compute a 256-row tile together: the even CTA takes
+// m-tile 2p, the odd CTA m-tile 2p+1 of the same (expert, n-tile). Each CTA
+// loads its own 128 rows of A and one half of the weight tile (MODE 0: the
+// gate rows in the even CTA, the up rows in the odd one; MODE 1: rows
+// [0,128) and [128,256) of the down tile), so each SM fetches 32 KB per 64-wide
+// K step instead of 48 KB for the same MMA work, and the ring gets 6 stages.
+// The even CTA issues every MMA (M=256, N=256) for the pair; both CTAs'
+// loads report to its full barrier, and its commits release the stages and
+// announce finished accumulators in both CTAs. Each CTA drains its own TMEM
+// rows; the odd CTA reports a drained accumulator to the even CTA remotely.
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;
+constexpr int P_B_BYTES = 128 * BK * 2;
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_ACC_BUFS = 2;
+constexpr int P_TMEM_COLS = ACC_COLS * P_ACC_BUFS;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 5;
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + P_NUM_BARS * 8 + 16 +
+                             2 * (MAX_EXPERTS + 1) * 4;
+constexpr uint32_t P_IDESC = ptx::idesc_bf16_f32(256, 256);
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
+                  const __grid_constant__ CUtensorMap tmB0,
+                  const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+  using namespace ptx;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base, sB = base + P_STAGES * P_A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + P_STAGES * P_STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + P_NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
+  int* seg_off = tile_start + (MAX_EXPERTS + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = args.n_experts;
+  const int KB = args.kdim / BK;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int first = static_cast<int>(cluster_id_x());
+  const int stride = static_cast<int>(cluster_count_x());
+  constexpr uint16_t kBoth = 0x3;
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + P_STAGES + s); };
+  auto bar_tfull = [&](int a) { return smem_u32(bars + 2 * P_STAGES + a); };
+  auto bar_tempty = [&](int a) { return smem_u32(bars + 2 * P_STAGES + 2 + a); };
+  const uint32_t bar_drain = smem_u32(bars + 2 * P_STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(bar_full(s), 1);   // even CTA: its producer's expect_tx arrive
+      mbar_init(bar_empty(s), 1);  // the even CTA's commit, multicast to both
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull(a), 1);
+      mbar_init(bar_tempty(a), 8);  // even CTA: 4 local + 4 remote epilogue warps
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    if (MODE == 0) prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), P_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 2) {
+    constexpr int PER = MAX_EXPERTS / 32;
+    int local[PER], sum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane * PER + j;
+      int tiles = 0;
+      if (e < N) {
+        const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
+        seg_off[e] = o0;
+        tiles = ((o1 - o0 + 2 * BM - 1) / (2 * BM)) * args.n_tiles;
+      }
+      local[j] = tiles;
+      sum += tiles;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane * PER + j;
+      if (e < N) tile_start[e] = run;
+      run += local[j];
+    }
+    if (lane == 31) tile_start[N] = incl;
+    if (lane == 0) seg_off[N] = args.offsets[N];
+  }
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tile_start[N];
+
+  auto decode = [&](int tile, int& e, int& m, int& n) {
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    e = lo;
+    const int mtp = (seg_off[e + 1] - seg_off[e] + 2 * BM - 1) / (2 * BM);
+    const int local = tile - tile_start[e];
+    n = local / mtp;
+    m = (local - n * mtp) * 2 + static_cast<int>(rank);
+  };
+  auto fail = [&]() {
+    set_status(args.status, MOE_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs) ----
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_parity = 0;
+    bool ok = true;
+    for (int tile = first; tile < total && ok; tile += stride) {
+      int e, m, n;
+      decode(tile, e, m, n);
+      const int row_a = seg_off[e] + m * BM;
+      const int row_b = e * args.b_rows + n * (MODE == 0 ? 128 : 256) +
+                        (MODE == 1 ? 128 * static_cast<int>(rank) : 0);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(bar_empty(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (leader) mbar_arrive_expect_tx(bar_full(stage), 2 * P_STAGE_BYTES);
+        const uint32_t full_leader = map_to_rank(bar_full(stage), 0);
+        tma_load_2d_pair(sA + stage * P_A_BYTES, &tmA, full_leader, kb * BK, row_a);
+        tma_load_2d_pair(sB + stage * P_B_BYTES, (MODE == 0 && !leader) ? &tmB1 : &tmB0,
+                         full_leader, kb * BK, row_b);
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == P_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      fail();
+      if (leader)  // the even CTA's full barriers count both CTAs' copies
+        for (int s = 0; s < P_STAGES; ++s)
+          if (issued & (1u << s))
+            mbar_wait_cluster(bar_full(s), (issued_parity >> s) & 1u, kWaitLimitNs, nullptr);
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------ MMA issuer (even CTA) ----
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued_any = false;
+    for (int tile = first; tile < total && ok; tile += stride) {
+      if (!mbar_wait_cluster(bar_tempty(acc), acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait_cluster(bar_full(stage), phase, kWaitLimitNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = sA + stage * P_A_BYTES, b0 = sB + stage * P_B_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32),
+                        sdesc_kmajor_sw128(b0 + kk * 32), P_IDESC, (kb | kk) != 0 ? 1u : 0u);
+        issued_any = true;
+        mma_commit_pair(bar_empty(stage), kBoth);
+        if (++stage == P_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit_pair(bar_tfull(acc), kBoth);
+      if (++acc == P_ACC_BUFS) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      fail();
+      if (issued_any) {
+        mma_commit_pair(bar_drain, 0x1);
+        mbar_wait(bar_drain, 0, kWaitLimitNs, nullptr);
+      }
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue (both CTAs) ----
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const uint32_t tempty_leader0 = map_to_rank(bar_tempty(0), 0);
+    const uint32_t tempty_leader1 = map_to_rank(bar_tempty(1), 0);
+    for (int tile = first; tile < total; tile += stride) {
+      int e, m, n;
+      decode(tile, e, m, n);
+      const int cnt = seg_off[e + 1] - seg_off[e];
+      bool ok = mbar_wait_cluster(bar_tfull(acc), acc_phase, kWaitLimitNs, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const int r = m * BM + q * 32 + lane;
+      const bool valid = r < cnt;
+      const size_t grow = static_cast<size_t>(seg_off[e]) + static_cast<size_t>(r);
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * ACC_COLS) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+      if (MODE == 0) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo + n * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + 128 + c * 32, u);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+            const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+            const float h0 = g0 / (1.f + __expf(-g0)) * u0;
+            const float h1 = g1 / (1.f + __expf(-g1)) * u1;
+            __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+            packed[j] = *reinterpret_cast<uint32_t*>(&hb);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                  packed[4 * v + 3]);
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(args.out) + grow * args.ldo + n * 256;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(out + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(bar_tempty(acc));
+        else mbar_arrive_remote(acc == 0 ? tempty_leader0 : tempty_leader1);
+      }
+      if (++acc == P_ACC_BUFS) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // no CTA of the pair leaves while the other may still signal it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, P_TMEM_COLS);
+  }
+}
+
 // ---- host side ---------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -369,8 +667,41 @@ bool set_smem_attr() {
       cudaFuncSetAttribute(grouped_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES) != cudaSuccess)
     return false;
+  if (cudaFuncSetAttribute(grouped_gemm_pair<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           P_SMEM_BYTES) != cudaSuccess ||
+      cudaFuncSetAttribute(grouped_gemm_pair<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           P_SMEM_BYTES) != cudaSuccess)
+    return false;
   if (dev < 31) done_mask |= 1 << dev;
   return true;
+}
+
+// CTA pairs pay off when experts have several 128-row tiles (then both CTAs
+// of a pair compute stored rows); with about one tile per expert the odd CTA
+// would mostly compute discarded rows.
+bool use_pairs(const moe_config& c, int64_t a_max) {
+  return a_max >= static_cast<int64_t>(c.n_experts) * BM * 4;
+}
+
+template <int MODE>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                        const TcArgs& args, int64_t pair_tiles, cudaStream_t s) {
+  const int sms = sm_count();
+  int64_t clusters = pair_tiles < sms / 2 ? pair_tiles : sms / 2;
+  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair<MODE>, a, b0, b1, args);
 }
 
 }  // namespace
@@ -385,16 +716,31 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
                          uint32_t* status, cudaStream_t s, int part) {
   if (a_max == 0) return MOE_OK;
   const int N = c.n_experts, d = c.d_model, F = c.d_ff;
+  const bool pairs = use_pairs(c, a_max);
   CUtensorMap mx, mg, mu, mh, md;
   if (!make_map(&mx, x_perm, a_max, d, 128) ||
       !make_map(&mg, w.w_gate, static_cast<uint64_t>(N) * F, d, 128) ||
       !make_map(&mu, w.w_up, static_cast<uint64_t>(N) * F, d, 128) ||
       !make_map(&mh, h, a_max, F, 128) ||
-      !make_map(&md, w.w_down, static_cast<uint64_t>(N) * d, F, 256))
+      !make_map(&md, w.w_down, static_cast<uint64_t>(N) * d, F, pairs ? 128 : 256))
     return MOE_ERR_CUDA;
   if (!set_smem_attr()) return MOE_ERR_CUDA;
   const int64_t mtiles = N + (a_max + BM - 1) / BM;  // upper bound on (expert, m-tile) pairs
   const int sms = sm_count();
+  if (pairs) {
+    const int64_t ptiles = N + (a_max + 2 * BM - 1) / (2 * BM);
+    if (part & 1) {
+      TcArgs a1{offsets, N, d, F / 128, F, h, F, status};
+      if (launch_pair<0>(mx, mg, mu, a1, ptiles * (F / 128), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    if (part & 2) {
+      TcArgs a2{offsets, N, F, d / 256, d, o, d, status};
+      if (launch_pair<1>(mh, md, md, a2, ptiles * (d / 256), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
   if (part & 1) {
     TcArgs a1{offsets, N, d, F / 128, F, h, F, status};
     const int64_t t1 = mtiles * (F / 128);

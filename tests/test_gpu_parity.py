@@ -39,6 +39,11 @@ SMALL = {
     "tc_top8_of_64": wl(T=257, d=512, F=256, N=64, K=8),
     "tc_one_token": wl(T=1, d=256, F=128, N=8, K=2),
     "tc_k3_odd_n": wl(T=200, d=256, F=128, N=7, K=3, capacity_factor=1.0),
+    # several 128-row tiles per expert: odd tile counts, ragged tails, capacity
+    "tc_many_tiles_odd": wl(T=1500, d=256, F=256, N=2, K=2),
+    "tc_many_tiles_capacity": wl(T=3000, d=512, F=128, N=4, K=1, capacity_factor=1.1,
+                            router_bias="skew", add_residual=True),
+    "tc_many_tiles_uneven": wl(T=2600, d=256, F=384, N=3, K=2, router_bias="skew"),
     # CUDA-core path: fp32, GELU, or shapes the tensor-core kernel does not tile
     "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
     "simt_gelu_nobias": wl(T=90, d=64, F=96, N=4, K=2, dtype="f32", activation="gelu",
