@@ -79,6 +79,9 @@ WsLayout ws_layout(const moe_config* c) {
   L.gate = take(T * K * 4);
   L.psum = take(nr * N * 4);
   L.pcnt = take(nr * N * 4);
+  const RouterTcPlan rp = router_tc_plan(*c);
+  L.w3 = take(rp.use ? static_cast<size_t>(3) * rp.NP * d * 2 : 0);
+  L.part = take(rp.use ? static_cast<size_t>(rp.S) * T * rp.NP * 4 : 0);
   L.ghist = take(K * nd * N * 4);
   L.gbase = take(K * nd * N * 4);
   L.offsets = take((N + 1) * 4);
@@ -114,6 +117,13 @@ moe_status check_ws(const moe_config* c, const void* ws) {
 
 uint8_t* at(void* ws, size_t off) {
   return static_cast<uint8_t*>(ws) + off;
+}
+
+RouterScratch router_scratch(void* ws, const WsLayout& L) {
+  return RouterScratch{reinterpret_cast<float*>(at(ws, L.psum)),
+                       reinterpret_cast<int32_t*>(at(ws, L.pcnt)),
+                       reinterpret_cast<__nv_bfloat16*>(at(ws, L.w3)),
+                       reinterpret_cast<float*>(at(ws, L.part))};
 }
 
 moe_status check_weights(const moe_config* c, const moe_expert_weights* w) {
@@ -211,8 +221,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r, con
       return MOE_ERR_INVALID;
     if (moe_status s = check_ws(cfg, ws)) return s;
     const WsLayout L = ws_layout(cfg);
-    return launch_router(*cfg, x, w_r, b_r, idx, gate, reinterpret_cast<float*>(at(ws, L.psum)),
-                         reinterpret_cast<int32_t*>(at(ws, L.pcnt)), stats,
+    return launch_router(*cfg, x, w_r, b_r, idx, gate, router_scratch(ws, L), stats,
                          static_cast<cudaStream_t>(stream));
   } catch (...) {
     return MOE_ERR_CUDA;
@@ -293,9 +302,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r, c
     void* x_perm = at(ws, L.x_perm);
     float* o = reinterpret_cast<float*>(at(ws, L.o));
     trace(0, s);
-    moe_status r = launch_router(*cfg, x, w_r, b_r, idx, gate,
-                                 reinterpret_cast<float*>(at(ws, L.psum)),
-                                 reinterpret_cast<int32_t*>(at(ws, L.pcnt)), stats, s);
+    moe_status r = launch_router(*cfg, x, w_r, b_r, idx, gate, router_scratch(ws, L), stats, s);
     if (r != MOE_OK) return r;
     trace(1, s);
     r = launch_dispatch(*cfg, x, idx, offsets, slot_of, tos, x_perm,

@@ -56,6 +56,8 @@ constexpr int kDispatchTokensPerBlock = 256; // tokens per dispatch block
 struct WsLayout {
   size_t idx, gate;           // [T][K] int32 / fp32 (moe_forward only)
   size_t psum, pcnt;          // router partials [nblk_r][N]
+  size_t w3, part;            // tensor-core router: W_r split [3][NP][d] bf16,
+                              // partial logits [S][T][NP] fp32
   size_t ghist, gbase;        // dispatch histograms [K][nblk_d][N]
   size_t offsets;             // [N+1] (moe_forward only)
   size_t slot_of;             // [T][K] (moe_forward only)
@@ -76,9 +78,29 @@ WsLayout ws_layout(const moe_config* c);
 int sm_count();
 
 // ---- launchers (each returns MOE_OK or MOE_ERR_CUDA) -----------------------
+// Tensor-core router plan: NP = experts padded to 32/64/128/256, NPT = experts
+// per tile, S = K splits of kb_per_split 64-wide steps each.
+struct RouterTcPlan {
+  bool use;
+  int NP, NPT, S, kb_per_split;
+};
+RouterTcPlan router_tc_plan(const moe_config& c);
+
+// Router scratch: per-block partial statistics (always), plus the weight
+// split and partial logits of the tensor-core router (NULL: CUDA-core router).
+struct RouterScratch {
+  float* psum;
+  int32_t* pcnt;
+  __nv_bfloat16* w3;
+  float* part;
+};
 moe_status launch_router(const moe_config& c, const void* x, const float* w_r,
-                         const float* b_r, int32_t* idx, float* gate, float* psum,
-                         int32_t* pcnt, const moe_stats* st, cudaStream_t s);
+                         const float* b_r, int32_t* idx, float* gate, const RouterScratch& sc,
+                         const moe_stats* st, cudaStream_t s);
+moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const void* x,
+                            const float* w_r, const float* b_r, int32_t* idx, float* gate,
+                            __nv_bfloat16* w3, float* part, float* psum, int32_t* pcnt,
+                            uint32_t* status, cudaStream_t s);
 
 moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* offsets, int32_t* slot_of, int32_t* token_of_slot,

@@ -16,6 +16,7 @@
 // shuffles. The contraction runs in fp32 FFMA (tf32 tensor cores would not
 // keep the logits accurate enough for bit-exact routing against float64).
 #include "moe_common.cuh"
+#include "router_select.cuh"
 
 #include <float.h>
 
@@ -26,6 +27,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+static_assert(kWarps == kSelectWarps, "router block shape");
 constexpr int BM = kRouterTokensPerBlock;  // 32 tokens per block
 
 // NPW: experts per warp (8: N <= 8, one token per lane; 32: 4 tokens x 8
@@ -127,87 +129,17 @@ router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
     const int t = t0 + tl;
     if (t >= T) break;
     float v[NJ];
-    bool bad = false;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       const int e = lane + 32 * j;
       v[j] = (e < N) ? red[tl * NP + e] : -INFINITY;
-      if (e < N && !isfinite(v[j])) bad = true;
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
-    // softmax over the N experts
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) m = fmaxf(m, v[j]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float p[NJ], s = 0.f;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      p[j] = (lane + 32 * j < N) ? expf(v[j] - m) : 0.f;
-      s += p[j];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const float inv = 1.f / s;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) pacc[j] += p[j] * inv;
-
-    // top-K: K rounds of a warp arg-max (largest logit, then lower index)
-    uint32_t taken = 0;
-    float sel_v = 0.f;
-    int sel_e = 0;
-    float top_v = 0.f, gsum = 0.f;
-    for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int be = INT32_MAX;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int e = lane + 32 * j;
-        const float vv = isnan(v[j]) ? -INFINITY : v[j];
-        if (e < N && !(taken & (1u << j)) && (vv > bv || (vv == bv && e < be))) {
-          bv = vv;
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (be < 0 || be >= N) be = 0;  // unreachable while K <= N; keeps indices in range
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (k == 0) top_v = bv;
-      const float g = expf(bv - top_v);
-      gsum += g;
-      if (lane == k) {
-        sel_v = g;
-        sel_e = be;
-      }
-    }
-    if (lane < K) {
-      idx_out[static_cast<size_t>(t) * K + lane] = sel_e;
-      gate_out[static_cast<size_t>(t) * K + lane] = sel_v / gsum;
-      atomicAdd(&scnt[sel_e], 1);
-    }
+    route_one_token<NJ>(v, N, K, static_cast<size_t>(t), lane, idx_out, gate_out, pacc, scnt,
+                        status);
   }
 
   // ---- phase D: per-block partials in a fixed order ----
-#pragma unroll
-  for (int j = 0; j < NJ; ++j)
-    if (lane + 32 * j < 256) pw[warp][lane + 32 * j] = pacc[j];
-  __syncthreads();
-  for (int e = tid; e < N; e += kThreads) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) s += pw[w][e];
-    psum[static_cast<size_t>(blockIdx.x) * N + e] = s;
-    pcnt[static_cast<size_t>(blockIdx.x) * N + e] = scnt[e];
-  }
+  write_block_stats<NJ>(pacc, pw, scnt, N, blockIdx.x, psum, pcnt);
 }
 
 // One block: count[e], P[e] = (1/T) sum_b psum[b][e] (b ascending),
@@ -261,18 +193,27 @@ cudaError_t launch_router_t(const moe_config& c, const Tx* x, const float* w_r, 
 }  // namespace
 
 moe_status launch_router(const moe_config& c, const void* x, const float* w_r, const float* b_r,
-                         int32_t* idx, float* gate, float* psum, int32_t* pcnt,
-                         const moe_stats* st, cudaStream_t s) {
+                         int32_t* idx, float* gate, const RouterScratch& sc, const moe_stats* st,
+                         cudaStream_t s) {
   if (c.T == 0) return MOE_OK;
   uint32_t* status = st ? st->status : nullptr;
-  cudaError_t err;
-  if (c.dtype == MOE_BF16)
-    err = launch_router_t(c, static_cast<const __nv_bfloat16*>(x), w_r, b_r, idx, gate, psum, pcnt,
-                          status, s);
-  else
-    err = launch_router_t(c, static_cast<const float*>(x), w_r, b_r, idx, gate, psum, pcnt,
-                          status, s);
-  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  float* psum = sc.psum;
+  int32_t* pcnt = sc.pcnt;
+  const RouterTcPlan plan = router_tc_plan(c);
+  if (plan.use && sc.w3 != nullptr && sc.part != nullptr) {
+    const moe_status r = launch_router_tc(c, plan, x, w_r, b_r, idx, gate, sc.w3, sc.part, psum,
+                                          pcnt, status, s);
+    if (r != MOE_OK) return r;
+  } else {
+    cudaError_t err;
+    if (c.dtype == MOE_BF16)
+      err = launch_router_t(c, static_cast<const __nv_bfloat16*>(x), w_r, b_r, idx, gate, psum,
+                            pcnt, status, s);
+    else
+      err = launch_router_t(c, static_cast<const float*>(x), w_r, b_r, idx, gate, psum, pcnt,
+                            status, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (st && (st->count || st->f || st->P || st->l_aux)) {
     const int nblk = (c.T + BM - 1) / BM;
     route_stats_kernel<<<1, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k, c.alpha,
@@ -353,7 +294,8 @@ extern "C" moe_status moe_route_no_workspace(const moe_config* cfg, const void* 
     float* psum = static_cast<float*>(scratch);
     int32_t* pcnt = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(scratch) +
                                                kRouteScratchElems * sizeof(float));
-    return launch_router(*cfg, x, w_r, b_r, idx, gate, psum, pcnt, stats,
+    const RouterScratch sc{psum, pcnt, nullptr, nullptr};  // CUDA-core router
+    return launch_router(*cfg, x, w_r, b_r, idx, gate, sc, stats,
                          static_cast<cudaStream_t>(stream));
   } catch (...) {
     return MOE_ERR_CUDA;

@@ -1,0 +1,116 @@
+// Per-token expert selection shared by the router kernels: softmax over the
+// N experts, top-K by logit (ties go to the lower expert index), gates =
+// softmax of the K selected logits, and the per-block partial sums of the
+// load-balance statistics.
+//
+// Sources: "MoE 混合专家模型稀疏激活的架构原理与负载均衡挑战" §三
+// MoERouter.forward (torch.topk on the logits, softmax of the top-k logits,
+// softmax(logits).mean(0) and the counts of the top-k indices for the
+// load-balance loss); "混合专家模型（Mixture of Experts, MoE）" 运行示例
+// (softmax, top-k, renormalised weights); "MoE 的核心思想" 具体数值示例.
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int kSelectWarps = 8;  // warps per router block (256 threads)
+
+// One warp holds one token's logits: lane owns experts lane + 32*j, j < NJ
+// (entries of experts >= N are ignored). Writes idx/gate of token t, adds the
+// token's softmax to pacc and counts the chosen experts in scnt (shared).
+template <int NJ>
+__device__ __forceinline__ void route_one_token(const float (&v)[NJ], int N, int K, size_t t,
+                                                int lane, int32_t* __restrict__ idx_out,
+                                                float* __restrict__ gate_out, float (&pacc)[NJ],
+                                                int32_t* scnt, uint32_t* status) {
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if (lane + 32 * j < N && !isfinite(v[j])) bad = true;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+  // softmax over the N experts
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if (lane + 32 * j < N) m = fmaxf(m, v[j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float p[NJ], s = 0.f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    p[j] = (lane + 32 * j < N) ? expf(v[j] - m) : 0.f;
+    s += p[j];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float inv = 1.f / s;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) pacc[j] += p[j] * inv;
+
+  // top-K: K rounds of a warp arg-max (largest logit, then lower index)
+  uint32_t taken = 0;
+  float sel_v = 0.f;
+  int sel_e = 0;
+  float top_v = 0.f, gsum = 0.f;
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int be = INT32_MAX;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      const float vv = isnan(v[j]) ? -INFINITY : v[j];
+      if (e < N && !(taken & (1u << j)) && (vv > bv || (vv == bv && e < be))) {
+        bv = vv;
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be < 0 || be >= N) be = 0;  // unreachable while K <= N; keeps indices in range
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (k == 0) top_v = bv;
+    const float g = expf(bv - top_v);
+    gsum += g;
+    if (lane == k) {
+      sel_v = g;
+      sel_e = be;
+    }
+  }
+  if (lane < K) {
+    idx_out[t * K + lane] = sel_e;
+    gate_out[t * K + lane] = sel_v / gsum;
+    atomicAdd(&scnt[sel_e], 1);
+  }
+}
+
+// Block-level partial statistics, summed over the block's warps in order:
+// psum[blk][e] = softmax mass of the block's tokens on e, pcnt[blk][e] =
+// their assignments to e. Every thread of the block calls this.
+template <int NJ>
+__device__ __forceinline__ void write_block_stats(const float (&pacc)[NJ], float (*pw)[256],
+                                                  const int32_t* scnt, int N, size_t blk,
+                                                  float* __restrict__ psum,
+                                                  int32_t* __restrict__ pcnt) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if (lane + 32 * j < 256) pw[warp][lane + 32 * j] = pacc[j];
+  __syncthreads();
+  for (int e = tid; e < N; e += blockDim.x) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSelectWarps; ++w) s += pw[w][e];
+    psum[blk * N + e] = s;
+    pcnt[blk * N + e] = scnt[e];
+  }
+}
+
+}  // namespace moe

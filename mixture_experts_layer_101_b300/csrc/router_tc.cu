@@ -1,0 +1,404 @@
+// Router logits on the tcgen05 tensor cores, exact to fp32 accuracy.
+//
+// Sources: "MoE 混合专家模型稀疏激活的架构原理与负载均衡挑战" §2.1 (logits =
+// x·W_r with W_r in R^{d x N}) and §三 MoERouter (weight stored (N, d),
+// logits = x @ W^T); "混合专家模型（Mixture of Experts, MoE）" 结构 2.
+//
+// The router weight is fp32; bf16 tensor cores multiply bf16 operands. Each
+// fp32 weight w is split exactly into three bf16 numbers, w = hi + mid + lo
+// (hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid); each residual
+// is exact in fp32 and the last one has at most 8 significant bits). x is
+// bf16, so every product x*hi, x*mid, x*lo is exact in the fp32 accumulator,
+// and x . W = x . hi + x . mid + x . lo is computed with fp32 accumulation
+// only: the same accuracy class as an fp32 FFMA dot product, which routing
+// that must match float64 needs (a 10-bit tf32 product would not do).
+//
+// Kernels:
+//   router_split_kernel  W_r [N][d] fp32 -> W3 [3][NP][d] bf16 (rows >= N zero)
+//   router_gemm_tc<NPT>  per (128-token tile, NPT-expert tile, K split):
+//                        part[s][t][e] = sum over the split's K of x[t] . W3[*][e]
+//                        (TMA ring of x and the three planes, tcgen05.mma
+//                        M=128 N=NPT K=16 into two alternating TMEM
+//                        accumulators, summed in fp32 registers)
+//   router_topk_kernel   per token: logits = sum_s part[s][t] (s ascending)
+//                        + b_r, then softmax / top-K / gates / statistics.
+// Accumulation length: the tensor core adds each product into the fp32
+// accumulator with less than round-to-nearest accuracy, so a long chain of
+// MMAs into one TMEM accumulator drifts (measured on the DeepSeek-shaped
+// router: gate error 2.3e-5 with 112 64-wide K steps per chain, 9e-7 with 2).
+// The MMA warp therefore restarts the accumulator every kChunkKb K steps,
+// alternating between two TMEM buffers, and the epilogue adds each finished
+// chunk into fp32 registers (round-to-nearest), overlapped with the next
+// chunk's MMAs. The K split gives enough CTAs for small T; chunk and split
+// sums are added in a fixed order, so results are deterministic.
+#include "moe_common.cuh"
+#include "ptx_sm100.cuh"
+#include "router_select.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int BM = 128, BK = 64;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kTargetCtas = 148;  // split K until the grid roughly fills a B300
+constexpr int kMaxSplits = 16;
+constexpr int kChunkKb = 2;  // 64-wide K steps per TMEM accumulation chain
+
+template <int NPT>
+struct Shape {
+  static constexpr int B_PLANE = NPT * BK * 2;           // one plane's tile
+  static constexpr int STAGE = A_BYTES + 3 * B_PLANE;     // x tile + 3 planes
+  static constexpr int STAGES = (NPT == 128) ? 3 : (NPT == 64 ? 5 : 6);
+  static constexpr int TMEM_COLS = 2 * NPT;  // two chunk accumulators
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + NUM_BARS * 8 + 16;
+  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, NPT);
+};
+
+__global__ void __launch_bounds__(256)
+router_split_kernel(const float* __restrict__ w_r, int N, int NP, int d,
+                    __nv_bfloat16* __restrict__ w3) {
+  const size_t total = static_cast<size_t>(NP) * d;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t e = i / d;
+    const float w = e < static_cast<size_t>(N) ? w_r[i] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    w3[i] = hi;
+    w3[total + i] = mid;
+    w3[2 * total + i] = __float2bfloat16_rn(r2);
+  }
+}
+
+struct GemmArgs {
+  int T, NP, KB, kb_per_split;
+  float* part;  // [S][T][NP]
+  uint32_t* status;
+};
+
+template <int NPT>
+__global__ void __launch_bounds__(kThreads, 1)
+router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+               const GemmArgs args) {
+  using namespace ptx;
+  using S = Shape<NPT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S::STAGES * S::STAGE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x, ntile = blockIdx.y, split = blockIdx.z;
+  const int kb0 = split * args.kb_per_split;
+  const int kb1 = min(args.KB, kb0 + args.kb_per_split);
+  const int nchunks = (kb1 - kb0 + kChunkKb - 1) / kChunkKb;
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + S::STAGES + s); };
+  auto bar_tfull = [&](int a) { return smem_u32(bars + 2 * S::STAGES + a); };
+  auto bar_tempty = [&](int a) { return smem_u32(bars + 2 * S::STAGES + 2 + a); };
+  const uint32_t bar_drain = smem_u32(bars + 2 * S::STAGES + 4);
+  auto stage_a = [&](int s) { return base + static_cast<uint32_t>(s * S::STAGE); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull(a), 1);
+      mbar_init(bar_tempty(a), 4);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto fail = [&]() {
+    set_status(args.status, MOE_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer: x tile + the three weight planes per stage ----
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_parity = 0;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(bar_empty(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+        fail();
+        for (int s = 0; s < S::STAGES; ++s)
+          if (issued & (1u << s))
+            mbar_wait(bar_full(s), (issued_parity >> s) & 1u, kWaitLimitNs, nullptr);
+        break;
+      }
+      mbar_arrive_expect_tx(bar_full(stage), S::STAGE);
+      const uint32_t a = stage_a(stage);
+      tma_load_2d(a, &tmX, bar_full(stage), kb * BK, m * BM);
+#pragma unroll
+      for (int p = 0; p < 3; ++p)
+        tma_load_2d(a + A_BYTES + p * S::B_PLANE, &tmW, bar_full(stage), kb * BK,
+                    p * args.NP + ntile * NPT);
+      issued |= 1u << stage;
+      issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == S::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer: chunks of kChunkKb K steps, alternating accumulators ----
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued_any = false;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NPT);
+      const int cb = kb0 + c * kChunkKb, ce = min(kb1, cb + kChunkKb);
+      for (int kb = cb; kb < ce; ++kb) {
+        if (!mbar_wait(bar_full(stage), phase, kWaitLimitNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = stage_a(stage);
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d_tmem, sdesc_kmajor_sw128(a + kk * 32),
+                     sdesc_kmajor_sw128(a + A_BYTES + p * S::B_PLANE + kk * 32), S::IDESC,
+                     (kb != cb || p != 0 || kk != 0) ? 1u : 0u);
+        issued_any = true;
+        mma_commit(bar_empty(stage));
+        if (++stage == S::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit(bar_tfull(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      fail();
+      if (issued_any) {
+        mma_commit(bar_drain);
+        mbar_wait(bar_drain, 0, kWaitLimitNs, nullptr);
+      }
+    }
+  } else if (warp >= 2) {
+    // ---- epilogue: add each finished chunk into fp32 registers ----
+    const int q = warp & 3;
+    float run[NPT];
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) run[j] = 0.f;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      ok = mbar_wait(bar_tfull(acc), acc_phase, kWaitLimitNs, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * NPT) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+      for (int cc = 0; cc < NPT / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(taddr + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) run[cc * 32 + j] += __uint_as_float(v[j]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      if (lane == 0) fail();
+    } else {
+      const int t = m * BM + q * 32 + lane;
+      if (t < args.T) {
+        float4* dst = reinterpret_cast<float4*>(
+            args.part + (static_cast<size_t>(split) * args.T + static_cast<size_t>(t)) * args.NP +
+            ntile * NPT);
+#pragma unroll
+        for (int j = 0; j < NPT / 4; ++j)
+          dst[j] = make_float4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+// Warp per token: logits = sum over the K splits in order + bias; then the
+// shared selection code. 32 tokens per 256-thread block.
+template <int NJ>
+__global__ void __launch_bounds__(256)
+router_topk_kernel(const float* __restrict__ part, int S, int NP, const float* __restrict__ b_r,
+                   int T, int N, int K, int32_t* __restrict__ idx_out,
+                   float* __restrict__ gate_out, float* __restrict__ psum,
+                   int32_t* __restrict__ pcnt, uint32_t* __restrict__ status) {
+  __shared__ float pw[kSelectWarps][256];
+  __shared__ int32_t scnt[256];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 256; i += blockDim.x) scnt[i] = 0;
+  __syncthreads();
+  float pacc[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) pacc[j] = 0.f;
+  const int t0 = blockIdx.x * kRouterTokensPerBlock;
+  for (int tl = warp; tl < kRouterTokensPerBlock; tl += kSelectWarps) {
+    const int t = t0 + tl;
+    if (t >= T) break;
+    float v[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      float acc = -INFINITY;
+      if (e < N) {
+        acc = 0.f;
+        for (int s = 0; s < S; ++s)
+          acc += part[(static_cast<size_t>(s) * T + t) * NP + e];
+        if (b_r != nullptr) acc += b_r[e];
+      }
+      v[j] = acc;
+    }
+    route_one_token<NJ>(v, N, K, static_cast<size_t>(t), lane, idx_out, gate_out, pacc, scnt,
+                        status);
+  }
+  write_block_stats<NJ>(pacc, pw, scnt, N, blockIdx.x, psum, pcnt);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NPT>
+cudaError_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, const GemmArgs& a,
+                        dim3 grid, cudaStream_t s) {
+  static std::mutex mu;
+  static int done_mask = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!(dev < 31 && (done_mask >> dev) & 1)) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          router_gemm_tc<NPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Shape<NPT>::SMEM);
+      if (e != cudaSuccess) return e;
+      if (dev < 31) done_mask |= 1 << dev;
+    }
+  }
+  router_gemm_tc<NPT><<<grid, kThreads, Shape<NPT>::SMEM, s>>>(mx, mw, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+RouterTcPlan router_tc_plan(const moe_config& c) {
+  RouterTcPlan p{};
+  p.use = c.dtype == MOE_BF16 && c.d_model % BK == 0 && c.T > 0;
+  if (!p.use) return p;
+  const int N = c.n_experts;
+  p.NP = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
+  p.NPT = p.NP > 128 ? 128 : p.NP;
+  const int KB = c.d_model / BK;
+  const int tiles = ((c.T + BM - 1) / BM) * (p.NP / p.NPT);
+  int S = kTargetCtas / tiles;
+  S = S < 1 ? 1 : (S > kMaxSplits ? kMaxSplits : S);
+  S = S > KB ? KB : S;
+  p.kb_per_split = (KB + S - 1) / S;
+  p.S = (KB + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
+  return p;
+}
+
+moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const void* x,
+                            const float* w_r, const float* b_r, int32_t* idx, float* gate,
+                            __nv_bfloat16* w3, float* part, float* psum, int32_t* pcnt,
+                            uint32_t* status, cudaStream_t s) {
+  const int N = c.n_experts, d = c.d_model, T = c.T;
+  router_split_kernel<<<sm_count() * 4, 256, 0, s>>>(w_r, N, p.NP, d, w3);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, x, static_cast<uint64_t>(T), d, BM) ||
+      !make_map(&mw, w3, static_cast<uint64_t>(3) * p.NP, d, p.NPT))
+    return MOE_ERR_CUDA;
+  GemmArgs a{T, p.NP, d / BK, p.kb_per_split, part, status};
+  const dim3 grid((T + BM - 1) / BM, p.NP / p.NPT, p.S);
+  cudaError_t e;
+  if (p.NPT == 128) e = launch_gemm<128>(mx, mw, a, grid, s);
+  else if (p.NPT == 64) e = launch_gemm<64>(mx, mw, a, grid, s);
+  else e = launch_gemm<32>(mx, mw, a, grid, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+  if (N <= 32)
+    router_topk_kernel<1><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, T, N, c.top_k, idx, gate,
+                                               psum, pcnt, status);
+  else if (N <= 64)
+    router_topk_kernel<2><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, T, N, c.top_k, idx, gate,
+                                               psum, pcnt, status);
+  else if (N <= 128)
+    router_topk_kernel<4><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, T, N, c.top_k, idx, gate,
+                                               psum, pcnt, status);
+  else
+    router_topk_kernel<8><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, T, N, c.top_k, idx, gate,
+                                               psum, pcnt, status);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe
