@@ -69,14 +69,11 @@ dispatch_scan_kernel(const int32_t* __restrict__ ghist, int nq, int N, int32_t C
   }
 }
 
-template <typename Tx>
 __global__ void __launch_bounds__(kThreads)
-dispatch_permute_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ idx, int T, int K,
-                        int N, int d, int32_t C, const int32_t* __restrict__ gbase,
-                        const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_of,
-                        int32_t* __restrict__ token_of_slot, Tx* __restrict__ x_perm) {
+dispatch_permute_kernel(const int32_t* __restrict__ idx, int T, int K, int N, int32_t C,
+                        const int32_t* __restrict__ gbase, const int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ slot_of, int32_t* __restrict__ token_of_slot) {
   __shared__ int32_t wcnt[kThreads / 32][256];
-  __shared__ int32_t sslot[kThreads];
   const int b = blockIdx.x, k = blockIdx.y, nb = gridDim.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < (kThreads / 32) * 256; i += kThreads) (&wcnt[0][0])[i] = 0;
@@ -104,19 +101,32 @@ dispatch_permute_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ id
     }
   }
   if (t < T) slot_of[static_cast<size_t>(t) * K + k] = slot;
-  sslot[tid] = slot;
-  __syncthreads();
+}
 
-  // gather: each warp copies the rows of its 32 assignments, 16 bytes a lane
+// x_perm[s] = x[token_of_slot[s]] for s < offsets[N]: one warp per slot, 16
+// bytes per lane per step, four steps in flight.
+template <typename Tx>
+__global__ void __launch_bounds__(256)
+dispatch_gather_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ token_of_slot,
+                       const int32_t* __restrict__ offsets, int N, int d, Tx* __restrict__ x_perm) {
+  const int total = offsets[N];
+  const int slot = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (slot >= total) return;
+  const int lane = threadIdx.x & 31;
+  const int t = token_of_slot[slot];
   const int chunks = d * static_cast<int>(sizeof(Tx)) / 16;
-  for (int i = 0; i < 32; ++i) {
-    const int s = sslot[warp * 32 + i];
-    if (s < 0) continue;
-    const int tt = b * kThreads + warp * 32 + i;
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(tt) * d);
-    uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(s) * d);
-    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
+  uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(slot) * d);
+  int c = lane;
+  for (; c + 96 < chunks; c += 128) {
+    const uint4 a = __ldg(src + c), b = __ldg(src + c + 32), e = __ldg(src + c + 64),
+                f = __ldg(src + c + 96);
+    dst[c] = a;
+    dst[c + 32] = b;
+    dst[c + 64] = e;
+    dst[c + 96] = f;
   }
+  for (; c < chunks; c += 32) dst[c] = __ldg(src + c);
 }
 
 }  // namespace
@@ -138,15 +148,22 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
                                          st ? st->n_dropped : nullptr);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   if (c.T > 0) {
-    if (c.dtype == MOE_BF16)
-      dispatch_permute_kernel<__nv_bfloat16><<<dim3(nb, K), kThreads, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(x), idx, c.T, K, N, c.d_model, C, gbase, offsets,
-          slot_of, token_of_slot, static_cast<__nv_bfloat16*>(x_perm));
-    else
-      dispatch_permute_kernel<float><<<dim3(nb, K), kThreads, 0, s>>>(
-          static_cast<const float*>(x), idx, c.T, K, N, c.d_model, C, gbase, offsets, slot_of,
-          token_of_slot, static_cast<float*>(x_perm));
+    dispatch_permute_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, C, gbase, offsets,
+                                                             slot_of, token_of_slot);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    const int64_t a_max = a_max_of(&c);
+    const unsigned gblocks = static_cast<unsigned>((a_max + 7) / 8);
+    if (gblocks > 0) {
+      if (c.dtype == MOE_BF16)
+        dispatch_gather_kernel<__nv_bfloat16><<<gblocks, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(x), token_of_slot, offsets, N, c.d_model,
+            static_cast<__nv_bfloat16*>(x_perm));
+      else
+        dispatch_gather_kernel<float><<<gblocks, 256, 0, s>>>(
+            static_cast<const float*>(x), token_of_slot, offsets, N, c.d_model,
+            static_cast<float*>(x_perm));
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
   }
   return MOE_OK;
 }

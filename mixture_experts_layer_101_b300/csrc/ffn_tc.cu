@@ -41,17 +41,31 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BK = 64, STAGES = 4, kThreads = 192;
+constexpr int BM = 128, BK = 64, kThreads = 192;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr int B_BYTES = 256 * BK * 2;   // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int ACC_COLS = 256;           // fp32 accumulator 128 x 256
-constexpr int TMEM_COLS = 512;          // two accumulators
+constexpr int ACC_COLS = 256;           // fp32 accumulator 128 x 256 (CTA-pair kernel)
 constexpr int MAX_EXPERTS = 256;
-constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
-                           2 * (MAX_EXPERTS + 1) * 4;
-constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, 256);
+
+// Tile shape of the one-CTA kernel. MODE 0 (gate/up): BNH output columns of
+// h per tile, i.e. BNH gate rows + BNH up rows of weights, MMA N = 2*BNH.
+// MODE 1 (down): BNH = 128, MMA N = 256 output columns. (Narrower gate/up
+// tiles, tried for small batches to even out the last wave, measured slower:
+// with 8 KB of weights per stage the single producer thread cannot keep the
+// loads in flight.)
+template <int MODE, int BNH>
+struct TcShape {
+  static constexpr int BN = 2 * BNH;                    // MMA N
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
+  static constexpr int ACC = BN;                        // TMEM columns per accumulator
+  static constexpr int TMEM_COLS = 2 * BN;              // two accumulators
+  static constexpr int NUM_BARS = 2 * STAGES + 5;       // full, empty, tfull[2], tempty[2], drain
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
+                              2 * (MAX_EXPERTS + 1) * 4;
+  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, BN);
+  static constexpr int OUT_COLS = MODE == 0 ? BNH : BN;  // output columns per tile
+};
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct TcArgs {
@@ -66,11 +80,16 @@ struct TcArgs {
 };
 
 // MODE 0: gate/up + SwiGLU -> h (bf16). MODE 1: down -> o (fp32).
-template <int MODE>
+template <int MODE, int BNH>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmA64,
+                const __grid_constant__ CUtensorMap tmA32,
+                const __grid_constant__ CUtensorMap tmA16, const TcArgs args) {
   using namespace ptx;
+  using Sh = TcShape<MODE, BNH>;
+  constexpr int STAGES = Sh::STAGES, B_BYTES = Sh::B_BYTES, STAGE_BYTES = Sh::STAGE_BYTES;
+  constexpr int NUM_BARS = Sh::NUM_BARS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -108,7 +127,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (MODE == 0) prefetch_tmap(&tmB1);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
     tmem_relinquish();
   }
   if (warp == 2) {
@@ -176,15 +195,21 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int e, m, n;
       decode(tile, e, m, n);
       const int row_a = seg_off[e] + m * BM;
-      const int row_b = e * args.b_rows + n * (MODE == 0 ? 128 : 256);
+      const int row_b = e * args.b_rows + n * Sh::OUT_COLS;
+      // Only the expert's rows of this tile are fetched (smallest box that
+      // covers them); the rest of the 128-row A tile keeps stale data, which
+      // only reaches accumulator rows that are never stored.
+      const int rows = min(BM, seg_off[e + 1] - row_a);
+      const CUtensorMap* mapA = rows > 64 ? &tmA : (rows > 32 ? &tmA64 : (rows > 16 ? &tmA32 : &tmA16));
+      const uint32_t a_bytes = static_cast<uint32_t>(rows > 64 ? 128 : (rows > 32 ? 64 : (rows > 16 ? 32 : 16))) * BK * 2;
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(bar_empty(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar_full(stage), STAGE_BYTES);
+        mbar_arrive_expect_tx(bar_full(stage), a_bytes + B_BYTES);
         const uint32_t a_dst = sA + stage * A_BYTES, b_dst = sB + stage * B_BYTES;
-        tma_load_2d(a_dst, &tmA, bar_full(stage), kb * BK, row_a);
+        tma_load_2d(a_dst, mapA, bar_full(stage), kb * BK, row_a);
         if (MODE == 0) {
           tma_load_2d(b_dst, &tmB0, bar_full(stage), kb * BK, row_b);
           tma_load_2d(b_dst + B_BYTES / 2, &tmB1, bar_full(stage), kb * BK, row_b);
@@ -216,7 +241,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Sh::ACC);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(bar_full(stage), phase, kWaitLimitNs, abort_flag)) {
           ok = false;
@@ -227,7 +252,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           mma_bf16(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32), sdesc_kmajor_sw128(b0 + kk * 32),
-                   IDESC, (kb | kk) != 0 ? 1u : 0u);
+                   Sh::IDESC, (kb | kk) != 0 ? 1u : 0u);
         issued_any = true;
         mma_commit(bar_empty(stage));
         if (++stage == STAGES) {
@@ -266,15 +291,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int r = m * BM + q * 32 + lane;
       const bool valid = r < cnt;
       const size_t grow = static_cast<size_t>(seg_off[e]) + static_cast<size_t>(r);
-      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * ACC_COLS) +
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * Sh::ACC) +
                              (static_cast<uint32_t>(q * 32) << 16);
       if (MODE == 0) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo + n * 128;
+        __nv_bfloat16* out =
+            static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo + n * Sh::OUT_COLS;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < BNH / 32; ++c) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + 128 + c * 32, u);
+          tmem_ld32(taddr + BNH + c * 32, u);
           tmem_ld_wait();
           uint32_t packed[16];
 #pragma unroll
@@ -295,9 +321,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
         }
       } else {
-        float* out = static_cast<float*>(args.out) + grow * args.ldo + n * 256;
+        float* out = static_cast<float*>(args.out) + grow * args.ldo + n * Sh::OUT_COLS;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < Sh::BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(taddr + c * 32, v);
           tmem_ld_wait();
@@ -323,7 +349,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, Sh::TMEM_COLS);
   }
 }
 
@@ -662,10 +688,10 @@ bool set_smem_attr() {
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 31 && (done_mask >> dev) & 1) return true;
-  if (cudaFuncSetAttribute(grouped_gemm_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_BYTES) != cudaSuccess ||
-      cudaFuncSetAttribute(grouped_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_BYTES) != cudaSuccess)
+  if (cudaFuncSetAttribute(grouped_gemm_tc<0, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           TcShape<0, 128>::SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(grouped_gemm_tc<1, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           TcShape<1, 128>::SMEM) != cudaSuccess)
     return false;
   if (cudaFuncSetAttribute(grouped_gemm_pair<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            P_SMEM_BYTES) != cudaSuccess ||
@@ -727,6 +753,11 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
   if (!set_smem_attr()) return MOE_ERR_CUDA;
   const int64_t mtiles = N + (a_max + BM - 1) / BM;  // upper bound on (expert, m-tile) pairs
   const int sms = sm_count();
+  CUtensorMap mx64, mx32, mx16, mh64, mh32, mh16;  // A boxes for partly filled tiles
+  if (!pairs && (!make_map(&mx64, x_perm, a_max, d, 64) || !make_map(&mx32, x_perm, a_max, d, 32) ||
+                 !make_map(&mx16, x_perm, a_max, d, 16) || !make_map(&mh64, h, a_max, F, 64) ||
+                 !make_map(&mh32, h, a_max, F, 32) || !make_map(&mh16, h, a_max, F, 16)))
+    return MOE_ERR_CUDA;
   if (pairs) {
     const int64_t ptiles = N + (a_max + 2 * BM - 1) / (2 * BM);
     if (part & 1) {
@@ -744,15 +775,15 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
   if (part & 1) {
     TcArgs a1{offsets, N, d, F / 128, F, h, F, status};
     const int64_t t1 = mtiles * (F / 128);
-    grouped_gemm_tc<0><<<static_cast<unsigned>(t1 < sms ? t1 : sms), kThreads, SMEM_BYTES, s>>>(
-        mx, mg, mu, a1);
+    grouped_gemm_tc<0, 128><<<static_cast<unsigned>(t1 < sms ? t1 : sms), kThreads,
+                              TcShape<0, 128>::SMEM, s>>>(mx, mg, mu, mx64, mx32, mx16, a1);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (part & 2) {
     TcArgs a2{offsets, N, F, d / 256, d, o, d, status};
     const int64_t t2 = mtiles * (d / 256);
-    grouped_gemm_tc<1><<<static_cast<unsigned>(t2 < sms ? t2 : sms), kThreads, SMEM_BYTES, s>>>(
-        mh, md, md, a2);
+    grouped_gemm_tc<1, 128><<<static_cast<unsigned>(t2 < sms ? t2 : sms), kThreads,
+                              TcShape<1, 128>::SMEM, s>>>(mh, md, md, mh64, mh32, mh16, a2);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;

@@ -142,33 +142,67 @@ router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
   write_block_stats<NJ>(pacc, pw, scnt, N, blockIdx.x, psum, pcnt);
 }
 
-// One block: count[e], P[e] = (1/T) sum_b psum[b][e] (b ascending),
-// f[e] = count/(T*K), L_aux = alpha*N*sum_e f[e]*P[e] (e ascending).
+// One block per expert e reduces the router blocks' partials psum[e][*] and
+// pcnt[e][*] (contiguous, coalesced): thread i sums blocks i, i+256, ... in
+// order, then fixed shuffle and shared-memory trees; every run adds in the
+// same order. Writes count[e], P[e] = sum / T, f[e] = count / (T*K), and
+// leaves the totals in psum[e][0], pcnt[e][0] for route_laux_kernel.
 __global__ void __launch_bounds__(256)
-route_stats_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pcnt, int nblk,
-                   int T, int N, int K, float alpha, int32_t* count, float* f, float* P,
-                   float* l_aux) {
-  __shared__ float fp[256];
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    float s = 0.f;
-    int32_t c = 0;
-    for (int b = 0; b < nblk; ++b) {
-      s += psum[static_cast<size_t>(b) * N + e];
-      c += pcnt[static_cast<size_t>(b) * N + e];
-    }
-    const float Pe = T > 0 ? s / static_cast<float>(T) : 0.f;
-    const float fe = T > 0 ? static_cast<float>(c) / (static_cast<float>(T) * K) : 0.f;
-    if (count) count[e] = c;
-    if (f) f[e] = fe;
-    if (P) P[e] = Pe;
-    fp[e] = fe * Pe;
+route_stats_kernel(float* __restrict__ psum, int32_t* __restrict__ pcnt, int nblk, int T, int N,
+                   int K, int32_t* count, float* f, float* P) {
+  __shared__ float ws_s[8];
+  __shared__ int32_t ws_c[8];
+  const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* ps = psum + static_cast<size_t>(e) * nblk;
+  const int32_t* pc = pcnt + static_cast<size_t>(e) * nblk;
+  float s = 0.f;
+  int32_t c = 0;
+  for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+    s += ps[b];
+    c += pc[b];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    c += __shfl_xor_sync(0xffffffffu, c, o);
+  }
+  if (lane == 0) {
+    ws_s[warp] = s;
+    ws_c[warp] = c;
   }
   __syncthreads();
-  if (threadIdx.x == 0 && l_aux) {
-    float s = 0.f;
-    for (int e = 0; e < N; ++e) s += fp[e];
-    *l_aux = alpha * static_cast<float>(N) * s;
+  if (threadIdx.x == 0) {
+    float st = 0.f;
+    int32_t ct = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+      st += ws_s[w];
+      ct += ws_c[w];
+    }
+    if (count) count[e] = ct;
+    if (f) f[e] = T > 0 ? static_cast<float>(ct) / (static_cast<float>(T) * K) : 0.f;
+    if (P) P[e] = T > 0 ? st / static_cast<float>(T) : 0.f;
+    psum[static_cast<size_t>(e) * nblk] = st;  // only this block reads row e
+    pcnt[static_cast<size_t>(e) * nblk] = ct;
   }
+}
+
+// L_aux = alpha * N * sum_e f[e] * P[e] from the per-expert totals that
+// route_stats_kernel left in psum[e][0], pcnt[e][0]. One warp: lane l adds
+// experts l, l+32, ... in order, then a fixed butterfly adds the lanes.
+__global__ void route_laux_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pcnt,
+                                  int nblk, int T, int N, int K, float alpha, float* l_aux) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+  for (int e = lane; e < N; e += 32) {
+    const float Pe = T > 0 ? psum[static_cast<size_t>(e) * nblk] / static_cast<float>(T) : 0.f;
+    const float fe = T > 0 ? static_cast<float>(pcnt[static_cast<size_t>(e) * nblk]) /
+                                 (static_cast<float>(T) * K)
+                           : 0.f;
+    s += fe * Pe;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) *l_aux = alpha * static_cast<float>(N) * s;
 }
 
 template <typename Tx>
@@ -216,9 +250,14 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
   }
   if (st && (st->count || st->f || st->P || st->l_aux)) {
     const int nblk = (c.T + BM - 1) / BM;
-    route_stats_kernel<<<1, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k, c.alpha,
-                                         st->count, st->f, st->P, st->l_aux);
+    route_stats_kernel<<<c.n_experts, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k,
+                                                   st->count, st->f, st->P);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (st->l_aux) {
+      route_laux_kernel<<<1, 32, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k, c.alpha,
+                                         st->l_aux);
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
   }
   return MOE_OK;
 }

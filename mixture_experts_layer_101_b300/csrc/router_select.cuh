@@ -91,9 +91,11 @@ __device__ __forceinline__ void route_one_token(const float (&v)[NJ], int N, int
   }
 }
 
-// Block-level partial statistics, summed over the block's warps in order:
-// psum[blk][e] = softmax mass of the block's tokens on e, pcnt[blk][e] =
-// their assignments to e. Every thread of the block calls this.
+// Block-level partial statistics, summed over the block's warps in order,
+// stored expert-major so that one expert's partials are contiguous:
+// psum[e][blk] = softmax mass of the block's tokens on e, pcnt[e][blk] =
+// their assignments to e (nblk = gridDim.x). Every thread of the block calls
+// this.
 template <int NJ>
 __device__ __forceinline__ void write_block_stats(const float (&pacc)[NJ], float (*pw)[256],
                                                   const int32_t* scnt, int N, size_t blk,
@@ -108,8 +110,8 @@ __device__ __forceinline__ void write_block_stats(const float (&pacc)[NJ], float
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < kSelectWarps; ++w) s += pw[w][e];
-    psum[blk * N + e] = s;
-    pcnt[blk * N + e] = scnt[e];
+    psum[static_cast<size_t>(e) * gridDim.x + blk] = s;
+    pcnt[static_cast<size_t>(e) * gridDim.x + blk] = scnt[e];
   }
 }
 

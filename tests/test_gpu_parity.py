@@ -44,6 +44,8 @@ SMALL = {
     "tc_many_tiles_capacity": wl(T=3000, d=512, F=128, N=4, K=1, capacity_factor=1.1,
                             router_bias="skew", add_residual=True),
     "tc_many_tiles_uneven": wl(T=2600, d=256, F=384, N=3, K=2, router_bias="skew"),
+    # enough tiles for the wide (128+128 column) gate/up tile of the one-CTA kernel
+    "tc_wide_tiles": wl(T=4096, d=256, F=1280, N=64, K=2),
     # CUDA-core path: fp32, GELU, or shapes the tensor-core kernel does not tile
     "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
     "simt_gelu_nobias": wl(T=90, d=64, F=96, N=4, K=2, dtype="f32", activation="gelu",
