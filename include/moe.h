@@ -251,6 +251,11 @@ moe_status moe_trace_events(void* const* events, int32_t n);
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char* moe_status_string(moe_status s);
 
+/* Number of kernels one moe_forward call on cfg launches (with every member
+ * of stats non-NULL), for accounting by benchmarks and tracers; -1 if cfg
+ * is invalid. Instrumentation; the pages have no counterpart. */
+int32_t moe_forward_launch_count(const moe_config* cfg);
+
 /* 1 if the expert FFN of cfg runs on the tcgen05 tensor-core path, 0 if it
  * runs on the CUDA-core path (fp32 configurations, or shapes whose d is not a
  * multiple of 64 or F not a multiple of 128), -1 if cfg is invalid. */

@@ -183,6 +183,17 @@ int32_t moe_capacity(const moe_config* cfg) {
   return capacity_of(cfg);
 }
 
+int32_t moe_forward_launch_count(const moe_config* cfg) {
+  if (!config_valid(cfg, nullptr)) return -1;
+  if (cfg->T == 0) return 1;  // the dispatch scan still writes offsets and counts
+  const int router = router_tc_plan(*cfg).use ? 3 : 1;  // (split, GEMM, top-K) or fused
+  const int stats = 2;                                  // per-expert reduction, L_aux
+  const int dispatch = 4;                               // histogram, scan, permute, gather
+  const int ffn = 2;                                    // gate/up, down
+  const int combine = 1;
+  return router + stats + dispatch + ffn + combine;
+}
+
 int32_t moe_ffn_uses_tensor_cores(const moe_config* cfg) {
   if (!config_valid(cfg, nullptr)) return -1;
   return ffn_tc_supported(*cfg) ? 1 : 0;

@@ -28,7 +28,7 @@ MOE_SWIGLU, MOE_GELU = 0, 1
 EXPORTED = ["moe_workspace_size", "moe_capacity", "moe_route", "moe_route_no_workspace",
             "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_status_string",
-            "moe_trace_events", "moe_ffn_uses_tensor_cores"]
+            "moe_trace_events", "moe_forward_launch_count", "moe_ffn_uses_tensor_cores"]
 
 
 class MoEError(RuntimeError):
@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_workspace_size.restype = ctypes.c_size_t
     lib.moe_capacity.argtypes = [cfgp]
     lib.moe_capacity.restype = ctypes.c_int32
+    lib.moe_forward_launch_count.argtypes = [cfgp]
+    lib.moe_forward_launch_count.restype = ctypes.c_int32
     lib.moe_ffn_uses_tensor_cores.argtypes = [cfgp]
     lib.moe_ffn_uses_tensor_cores.restype = ctypes.c_int32
     lib.moe_status_string.argtypes = [ctypes.c_int]
@@ -213,6 +215,14 @@ def ffn_uses_tensor_cores(cfg: LayerConfig) -> bool:
 
 
 moe_ffn_uses_tensor_cores = ffn_uses_tensor_cores
+
+
+def forward_launch_count(cfg: LayerConfig) -> int:
+    """Kernels one moe_forward launches for cfg (all statistics requested)."""
+    return int(load_library().moe_forward_launch_count(ctypes.byref(cfg.c())))
+
+
+moe_forward_launch_count = forward_launch_count
 
 
 def a_max(cfg: LayerConfig) -> int:
@@ -373,3 +383,45 @@ class MoELayer:
         self.forward(x_dev, stream)
         y_host.copy_(self.y, non_blocking=True)
         return self.stats.l_aux.to("cpu", non_blocking=True)
+
+    def forward_host_stream(self, x_hosts, y_hosts, laux_host):
+        """Runs the layer on a sequence of pinned host batches: y_hosts[i] =
+        layer(x_hosts[i]) and laux_host[i] = its L_aux. The host-to-device copy
+        of batch i+1 and the device-to-host copy of batch i-1 run on their own
+        streams while batch i computes (two device buffers for x, y and the
+        statistics). Returns when every copy has landed."""
+        n = len(x_hosts)
+        if n == 0:
+            return
+        dev = self.ws.device
+        cfg = self.cfg
+        if not hasattr(self, "_pipe"):
+            mk = lambda: torch.empty((cfg.T, cfg.d_model), dtype=cfg.torch_dtype, device=dev)
+            self._pipe = {"x": [mk(), mk()], "y": [mk(), mk()],
+                          "stats": [Stats(cfg.n_experts, dev), Stats(cfg.n_experts, dev)],
+                          "s_in": torch.cuda.Stream(dev), "s_out": torch.cuda.Stream(dev)}
+        p = self._pipe
+        comp = torch.cuda.current_stream(dev)
+        in_done = [torch.cuda.Event(), torch.cuda.Event()]
+        comp_done = [torch.cuda.Event(), torch.cuda.Event()]
+        out_done = [torch.cuda.Event(), torch.cuda.Event()]
+        for b in range(2):  # buffers start free
+            comp_done[b].record(comp)
+            out_done[b].record(comp)
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(p["s_in"]):
+                p["s_in"].wait_event(comp_done[b])        # batch i-2 no longer reads x[b]
+                p["x"][b].copy_(x_hosts[i], non_blocking=True)
+                in_done[b].record(p["s_in"])
+            comp.wait_event(in_done[b])
+            comp.wait_event(out_done[b])                  # y[b] of batch i-2 copied out
+            moe_forward(cfg, p["x"][b], self.w_r, self.b_r, self.weights, p["y"][b],
+                        p["stats"][b], self.ws, comp)
+            comp_done[b].record(comp)
+            with torch.cuda.stream(p["s_out"]):
+                p["s_out"].wait_event(comp_done[b])
+                y_hosts[i].copy_(p["y"][b], non_blocking=True)
+                laux_host[i:i + 1].copy_(p["stats"][b].l_aux, non_blocking=True)
+                out_done[b].record(p["s_out"])
+        p["s_out"].synchronize()

@@ -119,6 +119,13 @@ def test_status_strings(lib):
     assert moe.status_string(99) == "unknown status"
 
 
+def test_launch_count(lib):
+    assert moe.forward_launch_count(cfg()) == 12          # tensor-core router
+    assert moe.forward_launch_count(cfg(dtype="f32")) == 10
+    assert moe.forward_launch_count(cfg(d_model=72)) == 10  # d % 64 != 0: CUDA-core router
+    assert moe.forward_launch_count(cfg(top_k=9, n_experts=16)) == -1
+
+
 def test_tensor_core_path_choice(lib):
     assert moe.ffn_uses_tensor_cores(cfg())
     assert moe.ffn_uses_tensor_cores(cfg(d_model=7168, d_ff=2048, n_experts=256, top_k=8))

@@ -204,3 +204,22 @@ def test_full_size_workload(name):
         assert summary["n_dropped"] > 0
     del inp
     torch.cuda.empty_cache()
+
+
+def test_host_stream_matches_forward():
+    """MoELayer.forward_host_stream (copies of neighbouring batches overlapped
+    with compute) gives the same bits as forward() batch by batch."""
+    w = SMALL["tc_ragged"]
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
+    g = torch.Generator().manual_seed(5)
+    xs = [torch.randn((w.T, w.d), generator=g).to(torch.bfloat16).pin_memory() for _ in range(5)]
+    ys = [torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory() for _ in range(5)]
+    laux = torch.empty(5, dtype=torch.float32).pin_memory()
+    layer.forward_host_stream(xs, ys, laux)
+    for i in range(5):
+        y = layer.forward(xs[i].cuda()).cpu()
+        torch.cuda.synchronize()
+        assert torch.equal(y, ys[i])
+        assert float(laux[i]) == float(layer.stats.l_aux.item())
