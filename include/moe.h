@@ -248,6 +248,16 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r,
  * Errors: MOE_ERR_INVALID (n outside [0, 6], or events NULL with n > 0). */
 moe_status moe_trace_events(void* const* events, int32_t n);
 
+/* Self-test of failure detection (the pages have no counterpart). Launches
+ * one thread that waits, with the same bounded wait every mbarrier wait of
+ * the tensor-core kernels uses, on an mbarrier that nothing arrives at; after
+ * limit_us microseconds of wall time it gives up, ORs (1u << MOE_ERR_TIMEOUT)
+ * into *status (device pointer) and returns normally. Nothing faults, traps
+ * or hangs. limit_us in [1, 10^7].
+ * Errors: MOE_ERR_INVALID (status NULL, limit out of range), MOE_ERR_CUDA. */
+moe_status moe_selftest_bounded_wait(uint32_t limit_us, uint32_t* status,
+                                     moe_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char* moe_status_string(moe_status s);
 

@@ -790,3 +790,34 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded wait used by every mbarrier wait of the tensor-core
+// kernels: one thread waits on an mbarrier that nothing will ever arrive at,
+// gives up after limit_ns, records MOE_ERR_TIMEOUT in the status word and the
+// kernel returns normally (the GPU context stays usable).
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, uint32_t* status) {
+  using namespace ptx;
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  if (!mbar_wait(smem_u32(&bar), 0, limit_ns, &abort_flag)) set_status(status, MOE_ERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_selftest_bounded_wait(uint32_t limit_us, uint32_t* status,
+                                                moe_stream_t stream) {
+  if (status == nullptr || limit_us == 0 || limit_us > 10000000u) return MOE_ERR_INVALID;
+  moe::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint64_t>(limit_us) * 1000u, status);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

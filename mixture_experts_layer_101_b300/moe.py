@@ -28,7 +28,8 @@ MOE_SWIGLU, MOE_GELU = 0, 1
 EXPORTED = ["moe_workspace_size", "moe_capacity", "moe_route", "moe_route_no_workspace",
             "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_status_string",
-            "moe_trace_events", "moe_forward_launch_count", "moe_ffn_uses_tensor_cores"]
+            "moe_trace_events", "moe_selftest_bounded_wait", "moe_forward_launch_count",
+            "moe_ffn_uses_tensor_cores"]
 
 
 class MoEError(RuntimeError):
@@ -77,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_workspace_size.restype = ctypes.c_size_t
     lib.moe_capacity.argtypes = [cfgp]
     lib.moe_capacity.restype = ctypes.c_int32
+    lib.moe_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P]
+    lib.moe_selftest_bounded_wait.restype = ctypes.c_int
     lib.moe_forward_launch_count.argtypes = [cfgp]
     lib.moe_forward_launch_count.restype = ctypes.c_int32
     lib.moe_ffn_uses_tensor_cores.argtypes = [cfgp]
@@ -353,6 +356,15 @@ class TraceEvents:
             self.close()
         except Exception:
             pass
+
+
+def moe_selftest_bounded_wait(limit_us: int, status, stream=None):
+    """Runs the bounded-wait self-test: a device wait that nothing satisfies
+    gives up after limit_us and sets the MOE_ERR_TIMEOUT bit in status (an
+    int32 CUDA tensor)."""
+    lib = load_library()
+    _check(lib.moe_selftest_bounded_wait(int(limit_us), _ptr(status), _stream(stream)),
+           "moe_selftest_bounded_wait")
 
 
 TRACE_STAGES = ["router", "dispatch", "ffn_gate_up", "ffn_down", "combine"]

@@ -223,3 +223,24 @@ def test_host_stream_matches_forward():
         torch.cuda.synchronize()
         assert torch.equal(y, ys[i])
         assert float(laux[i]) == float(layer.stats.l_aux.item())
+
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """Failure detection without a fault: a device wait that nothing will
+    satisfy ends after its limit, the status word carries MOE_ERR_TIMEOUT, and
+    the context stays usable for a normal forward afterwards."""
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    moe.moe_selftest_bounded_wait(20000, status)       # 20 ms
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status.item()) & (1 << moe.moe.MOE_ERR_TIMEOUT)
+    assert 0.015 < elapsed < 5.0
+    w = SMALL["tc_ragged"]
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
+    layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert layer.stats.status_bits() == 0
