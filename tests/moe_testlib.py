@@ -9,7 +9,11 @@ Comparison rules:
     compared against the oracle re-run on the GPU's routing;
   * counts, kept, offsets, slots, token order and the drop set: bit-exact;
   * gates: |err| <= 1e-5; P and L_aux: relative error <= 1e-5;
-  * y: max |err| <= 1e-4 * rms(y) for fp32 layers, <= 2e-2 * rms(y) for bf16.
+  * y: max |err| <= 1e-4 * rms(y) for fp32 layers, <= 2e-2 * rms(y) for bf16
+    (the bars of the five named workloads); for random bf16 layers, where K=1
+    or small outputs leave nothing to average the bf16 roundings of h and y,
+    each element must lie within the bound those roundings allow
+    (bf16_rounding_bound).
 """
 from __future__ import annotations
 
@@ -90,7 +94,41 @@ def check_routing(l64: np.ndarray, idx_gpu: np.ndarray, K: int):
     return int(near.sum()), int(diff.sum())
 
 
-def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None, check_o=True):
+def bf16_rounding_bound(cfg: moe.LayerConfig, inp: dict, ref: dict) -> np.ndarray:
+    """Per-element bound [len(tokens)][d] on |y_gpu - y| that bf16 storage
+    alone allows: h is rounded to bf16 once (relative error <= 2^-9 per
+    element, which reaches o as at most 2^-9 * sum_f |W_down[j, f]| |h_f|),
+    y is rounded to bf16 once (<= 2^-8 |y|, one ulp), plus 1e-3 * rms(y) for
+    fp32 accumulation order and gate rounding."""
+    x = O.f64(inp["x"])
+    tok = ref["tokens"]
+    bound = np.zeros((len(tok), cfg.d_model))
+    reader = expert_reader(inp["experts"])
+    rows = {}
+    for i, t in enumerate(tok):
+        for k in range(cfg.top_k):
+            if ref["slot_of"][t, k] >= 0:
+                rows.setdefault(int(ref["idx"][t, k]), []).append((i, int(t), k))
+    for e, lst in rows.items():
+        ew = {kk: O.f64(v) for kk, v in reader(e).items() if v is not None}
+        xe = x[[t for (_, t, _) in lst]]
+        if cfg.activation == "swiglu":
+            h = O.silu(xe @ ew["w_gate"].T) * (xe @ ew["w_up"].T)
+            wd = ew["w_down"]
+        else:
+            z = xe @ ew["w1"].T + (ew["b1"][None, :] if "b1" in ew else 0.0)
+            h = O.gelu_erf(z)
+            wd = ew["w2"]
+        scale = np.abs(h) @ np.abs(wd).T * 2.0 ** -9
+        for r, (i, t, k) in enumerate(lst):
+            bound[i] += ref["gate"][t, k] * scale[r]
+    y = ref["y"]
+    rms = float(np.sqrt(np.mean(y ** 2))) if y.size else 0.0
+    return bound + 2.0 ** -8 * np.abs(y) + 1e-3 * rms
+
+
+def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
+                bound: str = "rms"):
     """Compare a stage-wise GPU run against the oracle. tokens: the tokens
     whose y is checked (None = all); routing, statistics and dispatch always
     cover every token. Returns a summary dict."""
@@ -127,6 +165,11 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None, chec
     y_ref = ref["y"]
     rms = float(np.sqrt(np.mean(y_ref ** 2))) if y_ref.size else 0.0
     err = float(np.max(np.abs(y_gpu - y_ref))) if y_ref.size else 0.0
-    assert err <= y_tolerance(cfg.dtype) * rms + 1e-30, (err, rms)
+    if bound == "rounding" and cfg.dtype == "bf16":
+        # per-element bound from the bf16 roundings the path performs
+        excess = np.abs(y_gpu - y_ref) - bf16_rounding_bound(cfg, inp, ref)
+        assert excess.max(initial=-1.0) <= 0.0, (err, rms, float(excess.max()))
+    else:
+        assert err <= y_tolerance(cfg.dtype) * rms + 1e-30, (err, rms)
     return {"near_ties": n_near, "routing_diff": n_diff, "A": A, "y_err_over_rms":
             err / rms if rms > 0 else 0.0, "n_dropped": ref["n_dropped"]}

@@ -244,3 +244,42 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     layer.forward(inp["x"])
     torch.cuda.synchronize()
     assert layer.stats.status_bits() == 0
+
+
+def _random_workloads(n=24, seed=2024):
+    """Seeded random layers inside the library's limits: both FFN paths, both
+    routers, capacity on and off, residual on and off, ragged T."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        tc = bool(rng.integers(0, 2))
+        N = int(rng.choice([1, 2, 3, 5, 8, 13, 32, 40, 64, 100, 256]))
+        K = int(rng.integers(1, min(N, 8) + 1))
+        if tc:
+            d = int(rng.choice([256, 512, 768]))
+            F = int(rng.choice([128, 256, 384]))
+            dtype, act, bias, init = "bf16", "swiglu", False, "normal"
+        else:
+            dtype = str(rng.choice(["bf16", "f32"]))
+            d = int(rng.choice([8, 24, 64, 72, 136])) if dtype == "bf16" else int(rng.choice([4, 12, 64, 100]))
+            F = int(rng.choice([4, 20, 64, 100]))
+            act = str(rng.choice(["swiglu", "gelu"]))
+            bias = act == "gelu" and bool(rng.integers(0, 2))
+            init = "uniform"
+        T = int(rng.integers(1, 700))
+        cf = float(rng.choice([np.inf, 0.5, 1.0, 1.25, 2.0]))
+        out.append(MoEWorkload(f"rand{i}", T=T, d=d, F=F, N=N, K=K, dtype=dtype, activation=act,
+                               has_bias=bias, init=init, capacity_factor=cf,
+                               add_residual=bool(rng.integers(0, 2)),
+                               router_bias=str(rng.choice(["none", "uniform"]))))
+    return out
+
+
+@pytest.mark.parametrize("w", _random_workloads(), ids=lambda w: w.name)
+def test_random_layers(w):
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    gpu = L.run_stages(cfg, inp)
+    L.check_layer(cfg, inp, gpu, bound="rounding")
+    y_fwd, _ = L.run_forward(cfg, inp)
+    assert torch.equal(y_fwd, gpu["y"])
