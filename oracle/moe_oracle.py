@@ -12,14 +12,14 @@ every stored input (bf16 or fp32) is promoted exactly to float64 and nothing
 is rounded on the way. Each function names the passage it follows. Sources:
 
   [MoE核心思想]  "MoE 的核心思想" (wmrh.cn): 公式表达重点, 具体数值示例,
-                 专家容量, 辅助损失公式.
+                 专家容量, 辅助损失公式, Router Z-Loss.
   [稀疏激活原理] "MoE 混合专家模型稀疏激活的架构原理与负载均衡挑战"
                  (mzlw.cn): §2.1, §2.2, §2.3, §三 (Expert, MoERouter,
                  MoELayer).
   [概念卡]       "混合专家模型（Mixture of Experts, MoE）" (learnagent.wiki):
-                 结构 2, 结构 3, 运行示例.
+                 结构 2, 结构 3, 结构 4, 运行示例.
   [替代FFN]      "MoE 如何替代 FFN？它解决了什么问题？带来哪些新挑战？"
-                 (mstx.cn): §1, §2.
+                 (mstx.cn): §1, §2, §4 (6).
 
 Readings where the pages are silent or disagree (each one is listed with its
 reason in the design notes):
@@ -33,7 +33,10 @@ reason in the design notes):
     renormalised again; with the residual on, the token passes as x;
   * f_i counts assignments before capacity, over T*K;
   * ties in top-K go to the lower expert index; selection compares logits;
-  * GELU is the exact-erf form.
+  * GELU is the exact-erf form;
+  * router z-loss (no formula on the pages) is the mean over tokens of the
+    squared log-sum-exp of the logits; the selection bias changes the top-K
+    choice only.
 
 Every function here is pinned by tests/test_oracle_pins.py against values
 the pages print, closed forms, special cases and brute force.
@@ -126,6 +129,48 @@ def gates_masked_softmax(l: np.ndarray, K: int):
     z = np.exp(masked - m)          # exp(-inf) = 0 outside the top K
     p = z / z.sum(axis=-1, keepdims=True)
     return idx, np.take_along_axis(p, idx, axis=-1)
+
+
+# --------------------------------------------------------------------------
+# gate variants (the further router options the pages name)
+# --------------------------------------------------------------------------
+def topk_with_selection_bias(l: np.ndarray, K: int, select_bias=None) -> np.ndarray:
+    """[概念卡] 结构 4 (auxiliary-loss-free balancing, DeepSeek-V3): a per-expert
+    bias, updated outside the gradient from how often each expert is chosen,
+    steers which experts are selected. It enters the top-K choice only; the
+    gates and the statistics use the unbiased logits. None = no bias."""
+    if select_bias is None:
+        return topk_experts(l, K)
+    return topk_experts(l + f64(select_bias)[None, :], K)
+
+
+def full_softmax_gates(l: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """[稀疏激活原理] §2.1 formula h(x) = Σ_{i∈TopK} softmax(logits)_i E_i(x):
+    the selected experts' probabilities under the softmax over all N experts,
+    not renormalised (the Switch-style gate; with K=1 it is the top
+    probability)."""
+    return np.take_along_axis(softmax(l), idx, axis=-1)
+
+
+def router_z_loss(l: np.ndarray) -> float:
+    """[MoE核心思想] Router Z-Loss: a penalty on the size of the router logits;
+    the page gives no formula. Read as the ST-MoE form, the mean over tokens
+    of (log Σ_e exp l[t, e])^2."""
+    if l.shape[0] == 0:
+        return 0.0
+    m = l.max(axis=-1)
+    lse = m + np.log(np.exp(l - m[:, None]).sum(axis=-1))
+    return float(np.mean(lse ** 2))
+
+
+def routing_entropy(p: np.ndarray) -> float:
+    """[替代FFN] §4 (6) monitors the routing entropy: the mean over tokens of
+    -Σ_e p[t, e] log p[t, e] (0 log 0 = 0)."""
+    if p.shape[0] == 0:
+        return 0.0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.where(p > 0, p * np.log(p), 0.0)
+    return float(np.mean(-t.sum(axis=-1)))
 
 
 # --------------------------------------------------------------------------
@@ -245,7 +290,8 @@ def stacked_expert(weights: dict, e: int) -> dict:
 # --------------------------------------------------------------------------
 def moe_forward(x, w_r, b_r, expert_of, *, K: int, activation: str,
                 capacity_factor: float = math.inf, alpha: float = 0.01,
-                add_residual: bool = False, tokens=None, idx_override=None):
+                add_residual: bool = False, tokens=None, idx_override=None,
+                gate_mode: str = "renorm", select_bias=None):
     """The whole layer in float64.
 
     expert_of(e) returns expert e's weights (dict of arrays, promoted here).
@@ -253,15 +299,23 @@ def moe_forward(x, w_r, b_r, expert_of, *, K: int, activation: str,
     dispatch always cover all tokens); None = all tokens.
     idx_override: use this routing instead of the oracle's top-K (to follow a
     GPU choice among near-tied logits); gates are recomputed from it.
+    gate_mode: "renorm" (softmax over the K selected logits) or "softmax"
+    (full-softmax probabilities, not renormalised). select_bias: [N] bias
+    for the top-K choice only.
     Returns a dict of every intermediate the layer defines."""
     xs = f64(x)
     T = xs.shape[0]
     l = router_logits(xs, w_r, b_r)
     N = l.shape[1]
     p = softmax(l) if T > 0 else np.zeros((0, N))
-    idx = topk_experts(l, K) if idx_override is None else np.asarray(idx_override,
-                                                                     dtype=np.int64)
-    gate = renormalised_gates(l, idx) if T > 0 else np.zeros((0, K))
+    idx = (topk_with_selection_bias(l, K, select_bias) if idx_override is None
+           else np.asarray(idx_override, dtype=np.int64))
+    if T == 0:
+        gate = np.zeros((0, K))
+    elif gate_mode == "renorm":
+        gate = renormalised_gates(l, idx)
+    else:
+        gate = full_softmax_gates(l, idx)
     count, f, P, l_aux = load_balance(idx, p, N, alpha)
     C = capacity(K, N, capacity_factor, T)
     disp = dispatch(idx, N, C)
@@ -288,7 +342,8 @@ def moe_forward(x, w_r, b_r, expert_of, *, K: int, activation: str,
                 acc = acc + gate[t, k] * o_of[(i, k)]
         y[i] = acc + (xs[t] if add_residual else 0.0)
     return {"logits": l, "p": p, "idx": idx, "gate": gate, "count": count, "f": f,
-            "P": P, "l_aux": l_aux, "C": C, "tokens": tok, "y": y, **{
+            "P": P, "l_aux": l_aux, "z_loss": router_z_loss(l), "entropy": routing_entropy(p),
+            "C": C, "tokens": tok, "y": y, **{
                 k: disp[k] for k in ("kept", "offsets", "slot_of", "token_of_slot",
                                      "rank_of", "n_dropped")}}
 

@@ -438,3 +438,78 @@ def test_switch_skew_bias_gives_seventy_percent():
     assert abs(share - 0.70) <= 0.005
     C = O.capacity(1, w.N, w.capacity_factor, w.T)
     assert C == 640
+
+
+# ------------------------------------------------------ gate variants ----
+def test_selection_bias_constant_shift_changes_nothing():
+    rng = np.random.default_rng(21)
+    l = rng.normal(size=(300, 16))
+    for K in (1, 2, 5):
+        a = O.topk_experts(l, K)
+        b = O.topk_with_selection_bias(l, K, np.full(16, 3.7))
+        assert np.array_equal(a, b)
+
+
+def test_selection_bias_forces_expert_but_gate_uses_unbiased_logits():
+    """[概念卡] 结构 4: a large bias on expert 3 puts it first in every top-2;
+    its renormalised gate is still exp(l3) / (exp(l3) + exp(l_other))."""
+    rng = np.random.default_rng(22)
+    x = rng.normal(size=(40, 6))
+    w_r = rng.normal(size=(5, 6))
+    bias = np.zeros(5)
+    bias[3] = 100.0
+    W = {"w_gate": rng.normal(size=(5, 7, 6)), "w_up": rng.normal(size=(5, 7, 6)),
+         "w_down": rng.normal(size=(5, 6, 7))}
+    r = O.moe_forward(x, w_r, None, lambda e: O.stacked_expert(W, e), K=2, activation="swiglu",
+                      select_bias=bias)
+    l = x @ w_r.T
+    assert np.all(r["idx"][:, 0] == 3)
+    other = r["idx"][:, 1]
+    lo = l[np.arange(40), other]
+    expect = np.exp(l[:, 3]) / (np.exp(l[:, 3]) + np.exp(lo))
+    assert np.max(np.abs(r["gate"][:, 0] - expect)) < 1e-14
+    # statistics ignore the bias: P is the mean unbiased softmax
+    assert np.max(np.abs(r["P"] - torch.softmax(torch.from_numpy(l), -1).numpy().mean(0))) < 1e-15
+
+
+def test_full_softmax_gates_closed_forms():
+    """[稀疏激活原理] §2.1 formula: g_i = softmax(logits)_i over all N."""
+    l = np.array([[0.0, math.log(2.0), math.log(3.0), -np.inf]])
+    idx = O.topk_experts(l, 2)
+    g = O.full_softmax_gates(l, idx)
+    assert list(idx[0]) == [2, 1]
+    assert np.allclose(g[0], [3 / 6, 2 / 6], atol=1e-15, rtol=0)
+    rng = np.random.default_rng(23)
+    l = rng.normal(size=(100, 7))
+    assert np.allclose(O.full_softmax_gates(l, O.topk_experts(l, 7)).sum(-1), 1.0, atol=1e-14)
+    top1 = O.full_softmax_gates(l, O.topk_experts(l, 1))[:, 0]
+    assert np.max(np.abs(top1 - O.softmax(l).max(-1))) < 1e-15
+
+
+def test_z_loss_closed_forms():
+    """Mean squared log-sum-exp: logits all c over N experts give (c + ln N)^2."""
+    for N, c in [(4, 0.0), (8, 1.5), (64, -2.0)]:
+        l = np.full((10, N), c)
+        assert abs(O.router_z_loss(l) - (c + math.log(N)) ** 2) < 1e-12
+    l = np.array([[1000.0, 0.0, 0.0]])  # one dominant logit: lse -> 1000
+    assert abs(O.router_z_loss(l) - 1000.0 ** 2) < 1e-6
+    rng = np.random.default_rng(24)
+    l = rng.normal(size=(50, 9)) * 3
+    ref = torch.logsumexp(torch.from_numpy(l), -1).numpy()
+    assert abs(O.router_z_loss(l) - float(np.mean(ref ** 2))) < 1e-12
+
+
+def test_routing_entropy_closed_forms():
+    assert abs(O.routing_entropy(O.softmax(np.zeros((5, 8)))) - math.log(8)) < 1e-15
+    assert O.routing_entropy(O.softmax(np.array([[0.0, -1e4, -1e4]]))) == 0.0
+    two = O.softmax(np.array([[2.0, 2.0, -np.inf, -np.inf]]))
+    assert abs(O.routing_entropy(two) - math.log(2)) < 1e-15
+
+
+def test_mutation_biased_gate_is_caught(monkeypatch):
+    orig = O.renormalised_gates
+    def wrong(l, idx):  # gates computed on the biased logits
+        return orig(l + np.eye(l.shape[1])[3] * 100.0, idx)
+    monkeypatch.setattr(O, "renormalised_gates", wrong)
+    with pytest.raises(AssertionError):
+        test_selection_bias_forces_expert_but_gate_uses_unbiased_logits()
