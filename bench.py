@@ -303,7 +303,8 @@ def time_oracle(w, x, w_r, b_r, experts, n_tokens):
     t0 = time.perf_counter()
     O.moe_forward(x, w_r, b_r, lambda e: {k: v[e] for k, v in experts.items()}, K=w.K,
                   activation=w.activation, capacity_factor=w.capacity_factor, alpha=w.alpha,
-                  add_residual=w.add_residual, tokens=range(n_tokens))
+                  add_residual=w.add_residual, tokens=range(n_tokens), gate_mode=w.gate_mode,
+                  select_bias=moe_inputs.make_select_bias(w))
     return time.perf_counter() - t0
 
 
@@ -333,7 +334,7 @@ def cpu_baseline(w, experts_dev, budget_s=15.0):
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
-    w = moe_inputs.WORKLOADS[args.workload]
+    w = selected_workload(args)
     x, w_r, b_r, experts = host_inputs(w)
     n = min(w.T, args.ref_tokens)
     for _ in range(args.warmup):
@@ -360,7 +361,8 @@ def workload_config(w, args, extra=None):
     cfg = {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.F, "n_experts": w.N,
            "top_k": w.K, "activation": w.activation, "capacity_factor":
            (None if math.isinf(w.capacity_factor) else w.capacity_factor),
-           "residual": w.add_residual, "parallelism": f"replicas x{args.gpus}",
+           "residual": w.add_residual, "gate_mode": w.gate_mode,
+           "select_bias": w.select_bias != "none", "parallelism": f"replicas x{args.gpus}",
            "l2": "256 MB written before every step, outside the step's event interval; "
                  "expert weights exceed L2"}
     if extra:
@@ -371,13 +373,22 @@ def workload_config(w, args, extra=None):
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
+def selected_workload(args):
+    import dataclasses
+    w = moe_inputs.WORKLOADS[args.workload]
+    return dataclasses.replace(w, gate_mode=args.gate_mode,
+                               select_bias="uniform" if args.select_bias else "none")
+
+
 def run_ours(args, world, rank):
     import mixture_experts_layer_101_b300 as moe
 
     moe.load_library()
-    w = moe_inputs.WORKLOADS[args.workload]
+    w = selected_workload(args)
     cfg = moe.LayerConfig.from_workload(w)
     dev = torch.device("cuda", torch.cuda.current_device())
+    sb = moe_inputs.make_select_bias(w)
+    cfg.select_bias = None if sb is None else sb.to(dev)
     x = moe_inputs.make_x(w).to(dev)
     w_r, b_r = moe_inputs.make_router(w)
     w_r = w_r.to(dev)
@@ -505,6 +516,10 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=256,
                     help="tokens whose experts the reference arm evaluates per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gate-mode", default="renorm", choices=["renorm", "softmax"],
+                    help="renorm: softmax over the K selected logits; softmax: full-softmax gate")
+    ap.add_argument("--select-bias", action="store_true",
+                    help="add a seeded top-K selection bias (auxiliary-loss-free balancing)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("at least 3 warm-up steps")

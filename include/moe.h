@@ -70,6 +70,13 @@ typedef enum {
 
 enum { MOE_F32 = 0, MOE_BF16 = 1 };      /* dtype of x, expert weights, y   */
 enum { MOE_SWIGLU = 0, MOE_GELU = 1 };   /* expert activation               */
+/* Gate of a selected expert:
+ *   MOE_GATE_RENORM   softmax over the K selected logits (default; [稀疏激活原理]
+ *                     §三 MoERouter, [概念卡] 运行示例, [MoE核心思想] 公式表达重点)
+ *   MOE_GATE_SOFTMAX  its probability under the softmax over all N experts,
+ *                     not renormalised ([稀疏激活原理] §2.1 formula; the Switch
+ *                     gate for K = 1)                                        */
+enum { MOE_GATE_RENORM = 0, MOE_GATE_SOFTMAX = 1 };
 
 /* Layer configuration (plain old data). */
 typedef struct {
@@ -85,6 +92,11 @@ typedef struct {
   float alpha;        /* coefficient of the load-balance loss               */
   int32_t add_residual; /* 1: y = x + sum_k g*E(x); a fully dropped token's
                            output is then x itself                          */
+  int32_t gate_mode;  /* MOE_GATE_RENORM | MOE_GATE_SOFTMAX                 */
+  const float* select_bias; /* DEVICE [N] fp32 or NULL: added to the logits for
+                           the top-K choice only; gates and statistics use the
+                           unbiased logits (auxiliary-loss-free balancing,
+                           [概念卡] 结构 4)                                    */
 } moe_config;
 
 /* Device-side statistics; every member is a caller-owned DEVICE pointer and
@@ -95,7 +107,12 @@ typedef struct {
  *   f[N]       count / (T*K)                            (fp32)
  *   P[N]       mean over tokens of the router softmax   (fp32)
  *   l_aux      alpha * N * sum_e f[e]*P[e]               (one fp32)
- *   status     device error bits, (1u << moe_status)     (one uint32)   */
+ *   status     device error bits, (1u << moe_status)     (one uint32)
+ *   z_loss     mean over tokens of (log sum_e exp l[t,e])^2 (one fp32):
+ *              the router z-loss ([MoE核心思想] Router Z-Loss, which gives no
+ *              formula; read as the squared log-sum-exp)
+ *   entropy    mean over tokens of -sum_e p log p        (one fp32):
+ *              the routing entropy ([替代FFN] §4 (6))                     */
 typedef struct {
   int32_t* count;
   int32_t* kept;
@@ -104,6 +121,8 @@ typedef struct {
   float* P;
   float* l_aux;
   uint32_t* status;
+  float* z_loss;
+  float* entropy;
 } moe_stats;
 
 /* Expert weights, stacked over experts, in the nn.Linear (out, in) layout of
@@ -145,7 +164,8 @@ int32_t moe_capacity(const moe_config* cfg);
  * 具体数值示例 (8 experts, top-2, gates 0.67 / 0.33).
  *   x    [T][d]  cfg->dtype        w_r [N][d] fp32      b_r [N] fp32 or NULL
  *   idx  [T][K]  int32 (out)       gate [T][K] fp32 (out)
- *   stats: count, f, P, l_aux, status are written (kept/n_dropped are not).
+ *   stats: count, f, P, l_aux, z_loss, entropy, status are written
+ *   (kept/n_dropped are not).
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE,
  * MOE_ERR_CUDA; device: MOE_ERR_NONFINITE. */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r,
@@ -160,8 +180,8 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r,
  * the statistics live in a fixed array inside the library (1 MiB, held on
  * every GPU that loads the library until the process exits) instead of a
  * caller workspace. Nothing is allocated: no cudaMalloc, no cudaFree.
- *   Limit: ceil(T / 32) * N <= 131072 (e.g. T <= 16384 with N = 256,
- *   T <= 524288 with N = 8); beyond it returns MOE_ERR_WORKSPACE before
+ *   Limit: ceil(T / 32) * (N + 2) <= 131072 (e.g. T <= 16256 with N = 256,
+ *   T <= 419424 with N = 8); beyond it returns MOE_ERR_WORKSPACE before
  *   launching anything.
  *   Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress) with that device current; make that first

@@ -29,6 +29,8 @@ bool config_valid(const moe_config* c, moe_status* why) {
   if (c->activation != MOE_SWIGLU && c->activation != MOE_GELU) return bad(MOE_ERR_INVALID);
   if ((c->has_bias != 0 && c->has_bias != 1) || (c->add_residual != 0 && c->add_residual != 1))
     return bad(MOE_ERR_INVALID);
+  if (c->gate_mode != MOE_GATE_RENORM && c->gate_mode != MOE_GATE_SOFTMAX)
+    return bad(MOE_ERR_INVALID);
   if (c->T < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0)
     return bad(MOE_ERR_INVALID);
   if (c->top_k > c->n_experts) return bad(MOE_ERR_INVALID);
@@ -77,7 +79,7 @@ WsLayout ws_layout(const moe_config* c) {
   const size_t A = static_cast<size_t>(L.a_max);
   L.idx = take(T * K * 4);
   L.gate = take(T * K * 4);
-  L.psum = take(nr * N * 4);
+  L.psum = take(nr * (N + 2) * 4);  // rows N, N+1: z-loss and entropy partials
   L.pcnt = take(nr * N * 4);
   const RouterTcPlan rp = router_tc_plan(*c);
   L.w3 = take(rp.use ? static_cast<size_t>(3) * rp.NP * d * 2 : 0);

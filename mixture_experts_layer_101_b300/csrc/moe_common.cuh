@@ -55,7 +55,7 @@ constexpr int kDispatchTokensPerBlock = 256; // tokens per dispatch block
 
 struct WsLayout {
   size_t idx, gate;           // [T][K] int32 / fp32 (moe_forward only)
-  size_t psum, pcnt;          // router partials [N][nblk_r] (expert-major)
+  size_t psum, pcnt;          // router partials [N+2][nblk_r], [N][nblk_r] (expert-major)
   size_t w3, part;            // tensor-core router: W_r split [3][NP][d] bf16,
                               // partial logits [S][T][NP] fp32
   size_t ghist, gbase;        // dispatch histograms [K][nblk_d][N]

@@ -35,7 +35,8 @@ constexpr int BM = kRouterTokensPerBlock;  // 32 tokens per block
 template <typename Tx, int NPW, int WS_N>
 __global__ void __launch_bounds__(kThreads)
 router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
-              const float* __restrict__ b_r, int T, int d, int N, int K,
+              const float* __restrict__ b_r, const float* __restrict__ sel_bias, int gate_mode,
+              int T, int d, int N, int K,
               int32_t* __restrict__ idx_out, float* __restrict__ gate_out,
               float* __restrict__ psum, int32_t* __restrict__ pcnt,
               uint32_t* __restrict__ status) {
@@ -49,6 +50,7 @@ router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
 
   __shared__ float red[WS_K * BM * NP];           // partial logits per d-slice
   __shared__ float pw[kWarps][256];               // per-warp probability sums
+  __shared__ float zh[2 * kWarps];                // per-warp z-loss / entropy sums
   __shared__ int32_t scnt[256];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -124,6 +126,7 @@ router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
   float pacc[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) pacc[j] = 0.f;
+  float zacc = 0.f, hacc = 0.f;
 
   for (int tl = warp; tl < BM; tl += kWarps) {
     const int t = t0 + tl;
@@ -134,12 +137,12 @@ router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
       const int e = lane + 32 * j;
       v[j] = (e < N) ? red[tl * NP + e] : -INFINITY;
     }
-    route_one_token<NJ>(v, N, K, static_cast<size_t>(t), lane, idx_out, gate_out, pacc, scnt,
-                        status);
+    route_one_token<NJ>(v, N, K, static_cast<size_t>(t), lane, sel_bias, gate_mode, idx_out,
+                        gate_out, pacc, zacc, hacc, scnt, status);
   }
 
   // ---- phase D: per-block partials in a fixed order ----
-  write_block_stats<NJ>(pacc, pw, scnt, N, blockIdx.x, psum, pcnt);
+  write_block_stats<NJ>(pacc, zacc, hacc, pw, zh, scnt, N, blockIdx.x, psum, pcnt);
 }
 
 // One block per expert e reduces the router blocks' partials psum[e][*] and
@@ -149,17 +152,18 @@ router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
 // leaves the totals in psum[e][0], pcnt[e][0] for route_laux_kernel.
 __global__ void __launch_bounds__(256)
 route_stats_kernel(float* __restrict__ psum, int32_t* __restrict__ pcnt, int nblk, int T, int N,
-                   int K, int32_t* count, float* f, float* P) {
+                   int K, int32_t* count, float* f, float* P, float* z_loss, float* entropy) {
   __shared__ float ws_s[8];
   __shared__ int32_t ws_c[8];
   const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool expert = e < N;  // rows N, N+1: z-loss and entropy sums
   const float* ps = psum + static_cast<size_t>(e) * nblk;
-  const int32_t* pc = pcnt + static_cast<size_t>(e) * nblk;
+  const int32_t* pc = pcnt + static_cast<size_t>(expert ? e : 0) * nblk;
   float s = 0.f;
   int32_t c = 0;
   for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
     s += ps[b];
-    c += pc[b];
+    if (expert) c += pc[b];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -178,9 +182,15 @@ route_stats_kernel(float* __restrict__ psum, int32_t* __restrict__ pcnt, int nbl
       st += ws_s[w];
       ct += ws_c[w];
     }
+    const float mean = T > 0 ? st / static_cast<float>(T) : 0.f;
+    if (!expert) {
+      float* dst = e == N ? z_loss : entropy;
+      if (dst) *dst = mean;
+      return;
+    }
     if (count) count[e] = ct;
     if (f) f[e] = T > 0 ? static_cast<float>(ct) / (static_cast<float>(T) * K) : 0.f;
-    if (P) P[e] = T > 0 ? st / static_cast<float>(T) : 0.f;
+    if (P) P[e] = mean;
     psum[static_cast<size_t>(e) * nblk] = st;  // only this block reads row e
     pcnt[static_cast<size_t>(e) * nblk] = ct;
   }
@@ -213,8 +223,9 @@ cudaError_t launch_router_t(const moe_config& c, const Tx* x, const float* w_r, 
   const int N = c.n_experts;
   dim3 grid(nblk), block(kThreads);
 #define MOE_ROUTER(NPW, WSN)                                                                  \
-  router_kernel<Tx, NPW, WSN><<<grid, block, 0, s>>>(x, w_r, b_r, c.T, c.d_model, N, c.top_k, \
-                                                     idx, gate, psum, pcnt, status)
+  router_kernel<Tx, NPW, WSN><<<grid, block, 0, s>>>(x, w_r, b_r, c.select_bias, c.gate_mode, \
+                                                     c.T, c.d_model, N, c.top_k, idx, gate,    \
+                                                     psum, pcnt, status)
   if (N <= 8) MOE_ROUTER(8, 1);
   else if (N <= 32) MOE_ROUTER(32, 1);
   else if (N <= 64) MOE_ROUTER(32, 2);
@@ -248,10 +259,11 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
                             status, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
-  if (st && (st->count || st->f || st->P || st->l_aux)) {
+  if (st && (st->count || st->f || st->P || st->l_aux || st->z_loss || st->entropy)) {
     const int nblk = (c.T + BM - 1) / BM;
-    route_stats_kernel<<<c.n_experts, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k,
-                                                   st->count, st->f, st->P);
+    route_stats_kernel<<<c.n_experts + 2, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts,
+                                                       c.top_k, st->count, st->f, st->P,
+                                                       st->z_loss, st->entropy);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     if (st->l_aux) {
       route_laux_kernel<<<1, 32, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k, c.alpha,
@@ -275,9 +287,10 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
 // partial sums held in the fixed array below instead of the workspace. The
 // array lives in every GPU that loads this library, until the process exits.
 //
-// Limit: ceil(T / 32) * N <= kRouteScratchElems (131072 = 1 MiB of scratch:
-// one fp32 and one int32 per (token block, expert)); larger requests return
-// MOE_ERR_WORKSPACE before anything is launched.
+// Limit: ceil(T / 32) * (N + 2) <= kRouteScratchElems (131072; 1 MiB of
+// scratch: one fp32 per (token block, expert or z-loss/entropy row) and one
+// int32 per (token block, expert)); larger requests return MOE_ERR_WORKSPACE
+// before anything is launched.
 //
 // Sharing: every call uses the same array. The router kernel writes every
 // partial it later reads, so nothing needs clearing between calls, but calls
@@ -327,7 +340,8 @@ extern "C" moe_status moe_route_no_workspace(const moe_config* cfg, const void* 
     if (!a16(x) || !a16(w_r) || !a16(idx) || !a16(gate) || (b_r && !a16(b_r)))
       return MOE_ERR_INVALID;
     const size_t nblk = (static_cast<size_t>(cfg->T) + BM - 1) / BM;
-    if (nblk * static_cast<size_t>(cfg->n_experts) > kRouteScratchElems) return MOE_ERR_WORKSPACE;
+    if (nblk * static_cast<size_t>(cfg->n_experts + 2) > kRouteScratchElems)
+      return MOE_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (moe_status s = route_scratch_address(&scratch)) return s;
     float* psum = static_cast<float*>(scratch);

@@ -18,12 +18,18 @@ constexpr int kSelectWarps = 8;  // warps per router block (256 threads)
 
 // One warp holds one token's logits: lane owns experts lane + 32*j, j < NJ
 // (entries of experts >= N are ignored). Writes idx/gate of token t, adds the
-// token's softmax to pacc and counts the chosen experts in scnt (shared).
+// token's softmax to pacc, counts the chosen experts in scnt (shared), and in
+// lane 0 adds the token's squared log-sum-exp to zacc and its routing entropy
+// to hacc. sel_bias (NULL or [N]) shifts the logits for the top-K choice
+// only ("混合专家模型（Mixture of Experts, MoE）" 结构 4); gate_mode picks the
+// renormalised or the full-softmax gate.
 template <int NJ>
 __device__ __forceinline__ void route_one_token(const float (&v)[NJ], int N, int K, size_t t,
-                                                int lane, int32_t* __restrict__ idx_out,
+                                                int lane, const float* __restrict__ sel_bias,
+                                                int gate_mode, int32_t* __restrict__ idx_out,
                                                 float* __restrict__ gate_out, float (&pacc)[NJ],
-                                                int32_t* scnt, uint32_t* status) {
+                                                float& zacc, float& hacc, int32_t* scnt,
+                                                uint32_t* status) {
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < NJ; ++j)
@@ -45,48 +51,85 @@ __device__ __forceinline__ void route_one_token(const float (&v)[NJ], int N, int
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   const float inv = 1.f / s;
+  float pv = 0.f;  // sum_e p_e * l_e, for the entropy lse - sum p l
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) pacc[j] += p[j] * inv;
+  for (int j = 0; j < NJ; ++j) {
+    pacc[j] += p[j] * inv;
+    if (p[j] > 0.f) pv += p[j] * inv * v[j];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) pv += __shfl_xor_sync(0xffffffffu, pv, o);
+  const float lse = m + logf(s);
+  if (lane == 0) {
+    zacc += lse * lse;
+    hacc += lse - pv;
+  }
 
-  // top-K: K rounds of a warp arg-max (largest logit, then lower index)
+  // top-K: K rounds of a warp arg-max of the (biased) selection key; ties go
+  // to the lower index; every lane records the unbiased logits selected
+  float key[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    const float vv = isnan(v[j]) ? -INFINITY : v[j];
+    key[j] = (sel_bias != nullptr && e < N) ? vv + sel_bias[e] : vv;
+  }
   uint32_t taken = 0;
-  float sel_v = 0.f;
+  float sel_u[8];
   int sel_e = 0;
-  float top_v = 0.f, gsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) sel_u[k] = -INFINITY;
   for (int k = 0; k < K; ++k) {
-    float bv = -INFINITY;
+    float bv = -INFINITY, bu = -INFINITY;
     int be = INT32_MAX;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       const int e = lane + 32 * j;
-      const float vv = isnan(v[j]) ? -INFINITY : v[j];
-      if (e < N && !(taken & (1u << j)) && (vv > bv || (vv == bv && e < be))) {
-        bv = vv;
+      if (e < N && !(taken & (1u << j)) && (key[j] > bv || (key[j] == bv && e < be))) {
+        bv = key[j];
         be = e;
+        bu = v[j];
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
       const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const float ou = __shfl_xor_sync(0xffffffffu, bu, o);
       if (ov > bv || (ov == bv && oe < be)) {
         bv = ov;
         be = oe;
+        bu = ou;
       }
     }
     if (be < 0 || be >= N) be = 0;  // unreachable while K <= N; keeps indices in range
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (k == 0) top_v = bv;
-    const float g = expf(bv - top_v);
-    gsum += g;
-    if (lane == k) {
-      sel_v = g;
-      sel_e = be;
-    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      if (kk == k) sel_u[kk] = bu;
+    if (lane == k) sel_e = be;
   }
   if (lane < K) {
+    float my_u = sel_u[0];
+#pragma unroll
+    for (int kk = 1; kk < 8; ++kk)
+      if (kk == lane) my_u = sel_u[kk];
+    float g;
+    if (gate_mode == MOE_GATE_SOFTMAX) {
+      g = expf(my_u - m) * inv;
+    } else {  // softmax over the K selected unbiased logits, summed in rank order
+      float msel = sel_u[0];
+#pragma unroll
+      for (int kk = 1; kk < 8; ++kk)
+        if (kk < K) msel = fmaxf(msel, sel_u[kk]);
+      float gsum = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        if (kk < K) gsum += expf(sel_u[kk] - msel);
+      g = expf(my_u - msel) / gsum;
+    }
     idx_out[t * K + lane] = sel_e;
-    gate_out[t * K + lane] = sel_v / gsum;
+    gate_out[t * K + lane] = g;
     atomicAdd(&scnt[sel_e], 1);
   }
 }
@@ -94,10 +137,12 @@ __device__ __forceinline__ void route_one_token(const float (&v)[NJ], int N, int
 // Block-level partial statistics, summed over the block's warps in order,
 // stored expert-major so that one expert's partials are contiguous:
 // psum[e][blk] = softmax mass of the block's tokens on e, pcnt[e][blk] =
-// their assignments to e (nblk = gridDim.x). Every thread of the block calls
-// this.
+// their assignments to e, psum[N][blk] / psum[N+1][blk] = their summed
+// squared log-sum-exp / entropy (nblk = gridDim.x). zh is a shared float[16].
+// Every thread of the block calls this.
 template <int NJ>
-__device__ __forceinline__ void write_block_stats(const float (&pacc)[NJ], float (*pw)[256],
+__device__ __forceinline__ void write_block_stats(const float (&pacc)[NJ], float zacc, float hacc,
+                                                  float (*pw)[256], float* zh,
                                                   const int32_t* scnt, int N, size_t blk,
                                                   float* __restrict__ psum,
                                                   int32_t* __restrict__ pcnt) {
@@ -105,13 +150,24 @@ __device__ __forceinline__ void write_block_stats(const float (&pacc)[NJ], float
 #pragma unroll
   for (int j = 0; j < NJ; ++j)
     if (lane + 32 * j < 256) pw[warp][lane + 32 * j] = pacc[j];
+  if (lane == 0) {
+    zh[warp] = zacc;
+    zh[kSelectWarps + warp] = hacc;
+  }
   __syncthreads();
+  const size_t nblk = gridDim.x;
   for (int e = tid; e < N; e += blockDim.x) {
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < kSelectWarps; ++w) s += pw[w][e];
-    psum[static_cast<size_t>(e) * gridDim.x + blk] = s;
-    pcnt[static_cast<size_t>(e) * gridDim.x + blk] = scnt[e];
+    psum[static_cast<size_t>(e) * nblk + blk] = s;
+    pcnt[static_cast<size_t>(e) * nblk + blk] = scnt[e];
+  }
+  if (tid < 2) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSelectWarps; ++w) s += zh[tid * kSelectWarps + w];
+    psum[static_cast<size_t>(N + tid) * nblk + blk] = s;
   }
 }
 

@@ -268,10 +268,11 @@ router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 template <int NJ>
 __global__ void __launch_bounds__(256)
 router_topk_kernel(const float* __restrict__ part, int S, int NP, const float* __restrict__ b_r,
-                   int T, int N, int K, int32_t* __restrict__ idx_out,
+                   const float* __restrict__ sel_bias, int gate_mode, int T, int N, int K, int32_t* __restrict__ idx_out,
                    float* __restrict__ gate_out, float* __restrict__ psum,
                    int32_t* __restrict__ pcnt, uint32_t* __restrict__ status) {
   __shared__ float pw[kSelectWarps][256];
+  __shared__ float zh[2 * kSelectWarps];
   __shared__ int32_t scnt[256];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 256; i += blockDim.x) scnt[i] = 0;
@@ -279,6 +280,7 @@ router_topk_kernel(const float* __restrict__ part, int S, int NP, const float* _
   float pacc[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) pacc[j] = 0.f;
+  float zacc = 0.f, hacc = 0.f;
   const int t0 = blockIdx.x * kRouterTokensPerBlock;
   for (int tl = warp; tl < kRouterTokensPerBlock; tl += kSelectWarps) {
     const int t = t0 + tl;
@@ -296,10 +298,10 @@ router_topk_kernel(const float* __restrict__ part, int S, int NP, const float* _
       }
       v[j] = acc;
     }
-    route_one_token<NJ>(v, N, K, static_cast<size_t>(t), lane, idx_out, gate_out, pacc, scnt,
-                        status);
+    route_one_token<NJ>(v, N, K, static_cast<size_t>(t), lane, sel_bias, gate_mode, idx_out,
+                        gate_out, pacc, zacc, hacc, scnt, status);
   }
-  write_block_stats<NJ>(pacc, pw, scnt, N, blockIdx.x, psum, pcnt);
+  write_block_stats<NJ>(pacc, zacc, hacc, pw, zh, scnt, N, blockIdx.x, psum, pcnt);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -387,16 +389,16 @@ moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const vo
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
   if (N <= 32)
-    router_topk_kernel<1><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, T, N, c.top_k, idx, gate,
+    router_topk_kernel<1><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, T, N, c.top_k, idx, gate,
                                                psum, pcnt, status);
   else if (N <= 64)
-    router_topk_kernel<2><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, T, N, c.top_k, idx, gate,
+    router_topk_kernel<2><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, T, N, c.top_k, idx, gate,
                                                psum, pcnt, status);
   else if (N <= 128)
-    router_topk_kernel<4><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, T, N, c.top_k, idx, gate,
+    router_topk_kernel<4><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, T, N, c.top_k, idx, gate,
                                                psum, pcnt, status);
   else
-    router_topk_kernel<8><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, T, N, c.top_k, idx, gate,
+    router_topk_kernel<8><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, T, N, c.top_k, idx, gate,
                                                psum, pcnt, status);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -23,6 +23,7 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
 MOE_ERR_TIMEOUT, MOE_ERR_NONFINITE, MOE_ERR_WORKSPACE, MOE_ERR_INDEX = 4, 5, 6, 7
 MOE_F32, MOE_BF16 = 0, 1
 MOE_SWIGLU, MOE_GELU = 0, 1
+MOE_GATE_RENORM, MOE_GATE_SOFTMAX = 0, 1
 
 # Every symbol the header declares, in declaration order.
 EXPORTED = ["moe_workspace_size", "moe_capacity", "moe_route", "moe_route_no_workspace",
@@ -43,13 +44,15 @@ class MoEConfig(ctypes.Structure):
                 ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("activation", ctypes.c_int32),
                 ("has_bias", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
-                ("alpha", ctypes.c_float), ("add_residual", ctypes.c_int32)]
+                ("alpha", ctypes.c_float), ("add_residual", ctypes.c_int32),
+                ("gate_mode", ctypes.c_int32), ("select_bias", ctypes.c_void_p)]
 
 
 class MoEStatsC(ctypes.Structure):
     _fields_ = [("count", ctypes.c_void_p), ("kept", ctypes.c_void_p),
                 ("n_dropped", ctypes.c_void_p), ("f", ctypes.c_void_p), ("P", ctypes.c_void_p),
-                ("l_aux", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+                ("l_aux", ctypes.c_void_p), ("status", ctypes.c_void_p),
+                ("z_loss", ctypes.c_void_p), ("entropy", ctypes.c_void_p)]
 
 
 class MoEExpertWeightsC(ctypes.Structure):
@@ -124,12 +127,15 @@ class LayerConfig:
     capacity_factor: float = math.inf
     alpha: float = 0.01
     add_residual: bool = False
+    gate_mode: str = "renorm"          # "renorm" | "softmax"
+    select_bias: torch.Tensor | None = None  # [N] fp32 CUDA tensor: top-K choice only
 
     @classmethod
     def from_workload(cls, w, T: int | None = None) -> "LayerConfig":
         return cls(T=w.T if T is None else T, d_model=w.d, d_ff=w.F, n_experts=w.N, top_k=w.K,
                    dtype=w.dtype, activation=w.activation, has_bias=w.has_bias,
-                   capacity_factor=w.capacity_factor, alpha=w.alpha, add_residual=w.add_residual)
+                   capacity_factor=w.capacity_factor, alpha=w.alpha, add_residual=w.add_residual,
+                   gate_mode=getattr(w, "gate_mode", "renorm"))
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -140,7 +146,9 @@ class LayerConfig:
                          MOE_BF16 if self.dtype == "bf16" else MOE_F32,
                          MOE_SWIGLU if self.activation == "swiglu" else MOE_GELU,
                          int(self.has_bias), float(self.capacity_factor), float(self.alpha),
-                         int(self.add_residual))
+                         int(self.add_residual),
+                         MOE_GATE_SOFTMAX if self.gate_mode == "softmax" else MOE_GATE_RENORM,
+                         _ptr(self.select_bias))
 
 
 def _ptr(t) -> int | None:
@@ -179,10 +187,13 @@ class Stats:
         self.P = torch.zeros(n_experts, dtype=f32, device=device)
         self.l_aux = torch.zeros(1, dtype=f32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.z_loss = torch.zeros(1, dtype=f32, device=device)
+        self.entropy = torch.zeros(1, dtype=f32, device=device)
 
     def c(self) -> MoEStatsC:
         return MoEStatsC(*(_ptr(t) for t in (self.count, self.kept, self.n_dropped, self.f,
-                                             self.P, self.l_aux, self.status)))
+                                             self.P, self.l_aux, self.status, self.z_loss,
+                                             self.entropy)))
 
     def status_bits(self) -> int:
         return int(self.status.item()) & 0xFFFFFFFF
@@ -191,7 +202,8 @@ class Stats:
         return {"count": self.count.cpu().numpy(), "kept": self.kept.cpu().numpy(),
                 "n_dropped": int(self.n_dropped.item()), "f": self.f.cpu().numpy(),
                 "P": self.P.cpu().numpy(), "l_aux": float(self.l_aux.item()),
-                "status": self.status_bits()}
+                "status": self.status_bits(), "z_loss": float(self.z_loss.item()),
+                "entropy": float(self.entropy.item())}
 
 
 def weights_c(weights: dict) -> MoEExpertWeightsC:

@@ -40,6 +40,7 @@ SWITCH_SKEW_EXPERTS = 4
 
 X_SEED = 0
 ROUTER_SEED = 1000
+SELECT_BIAS_SEED = 1001
 
 
 def expert_seed(e: int) -> int:
@@ -64,6 +65,8 @@ class MoEWorkload:
     init: str = "normal"         # "normal" (std w_std) | "uniform" (1/sqrt(fan_in))
     w_std: float = 0.02
     router_std: float = 0.02
+    gate_mode: str = "renorm"    # "renorm" | "softmax"
+    select_bias: str = "none"    # "none" | "uniform": a top-K selection bias
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -124,6 +127,15 @@ def make_router(w: MoEWorkload, skew_bias: float | None = None):
         b_r = torch.zeros(w.N, dtype=torch.float32)
         b_r[:SWITCH_SKEW_EXPERTS] = beta
     return w_r.contiguous(), (None if b_r is None else b_r.contiguous())
+
+
+def make_select_bias(w: MoEWorkload):
+    """Top-K selection bias [N] fp32 on the CPU (None unless requested):
+    U(-0.5, 0.5), seed 1001."""
+    if w.select_bias == "none":
+        return None
+    g = _gen(SELECT_BIAS_SEED, "cpu")
+    return _uniform((w.N,), 0.5, g, "cpu").contiguous()
 
 
 def make_expert(w: MoEWorkload, e: int, device="cpu") -> dict:

@@ -37,9 +37,16 @@ def device_inputs(w: moe_inputs.MoEWorkload):
     """Inputs on cuda:0; x and the router drawn on the CPU, experts on the GPU."""
     x = moe_inputs.make_x(w)
     w_r, b_r = moe_inputs.make_router(w)
+    sb = moe_inputs.make_select_bias(w)
     experts = moe_inputs.make_experts(w, "cuda")
     return {"x": x.cuda(), "w_r": w_r.cuda(), "b_r": None if b_r is None else b_r.cuda(),
-            "experts": experts}
+            "select_bias": None if sb is None else sb.cuda(), "experts": experts}
+
+
+def layer_config(w: moe_inputs.MoEWorkload, inp: dict) -> moe.LayerConfig:
+    cfg = moe.LayerConfig.from_workload(w)
+    cfg.select_bias = inp.get("select_bias")
+    return cfg
 
 
 def expert_reader(experts: dict):
@@ -134,13 +141,15 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
     cover every token. Returns a summary dict."""
     K, N = cfg.top_k, cfg.n_experts
     x, w_r, b_r = inp["x"].cpu(), inp["w_r"].cpu(), None if inp["b_r"] is None else inp["b_r"].cpu()
+    sb = None if cfg.select_bias is None else cfg.select_bias.cpu()
     l64 = O.router_logits(x, w_r, b_r)
+    key64 = l64 if sb is None else l64 + O.f64(sb)[None, :]  # what the top-K compares
     idx_gpu = gpu["idx"].numpy().astype(np.int64)
-    n_near, n_diff = check_routing(l64, idx_gpu, K)
+    n_near, n_diff = check_routing(key64, idx_gpu, K)
     ref = O.moe_forward(x, w_r, b_r, expert_reader(inp["experts"]), K=K,
                         activation=cfg.activation, capacity_factor=cfg.capacity_factor,
                         alpha=cfg.alpha, add_residual=cfg.add_residual, tokens=tokens,
-                        idx_override=idx_gpu)
+                        idx_override=idx_gpu, gate_mode=cfg.gate_mode, select_bias=sb)
     # gates and statistics
     assert np.max(np.abs(gpu["gate"].numpy() - ref["gate"]), initial=0) <= GATE_TOL
     st = gpu["stats"]
@@ -148,6 +157,8 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
     assert np.allclose(st["P"], ref["P"], rtol=STAT_RTOL, atol=1e-7)
     assert np.allclose(st["f"], ref["f"], rtol=1e-6, atol=0)
     assert abs(st["l_aux"] - ref["l_aux"]) <= STAT_RTOL * abs(ref["l_aux"]) + 1e-9
+    assert abs(st["z_loss"] - ref["z_loss"]) <= STAT_RTOL * abs(ref["z_loss"]) + 1e-6
+    assert abs(st["entropy"] - ref["entropy"]) <= STAT_RTOL * abs(ref["entropy"]) + 1e-6
     assert st["status"] == 0
     # dispatch: bit-exact
     assert np.array_equal(st["kept"], ref["kept"])

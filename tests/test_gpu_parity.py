@@ -46,6 +46,13 @@ SMALL = {
     "tc_many_tiles_uneven": wl(T=2600, d=256, F=384, N=3, K=2, router_bias="skew"),
     # enough tiles for the wide (128+128 column) gate/up tile of the one-CTA kernel
     "tc_wide_tiles": wl(T=4096, d=256, F=1280, N=64, K=2),
+    # gate variants: full-softmax (Switch) gates, top-K selection bias
+    "tc_softmax_gate": wl(T=300, d=256, F=256, N=8, K=2, gate_mode="softmax"),
+    "tc_select_bias": wl(T=500, d=256, F=128, N=16, K=4, select_bias="uniform"),
+    "tc_switch_gate_capacity": wl(T=1000, d=256, F=128, N=8, K=1, gate_mode="softmax",
+                                  capacity_factor=1.25, add_residual=True),
+    "simt_softmax_bias_fp32": wl(T=100, d=36, F=52, N=6, K=3, dtype="f32", init="uniform",
+                                 gate_mode="softmax", select_bias="uniform"),
     # CUDA-core path: fp32, GELU, or shapes the tensor-core kernel does not tile
     "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
     "simt_gelu_nobias": wl(T=90, d=64, F=96, N=4, K=2, dtype="f32", activation="gelu",
@@ -61,8 +68,8 @@ SMALL = {
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_layers_stagewise(name):
     w = SMALL[name]
-    cfg = moe.LayerConfig.from_workload(w)
     inp = L.device_inputs(w)
+    cfg = L.layer_config(w, inp)
     gpu = L.run_stages(cfg, inp)
     summary = L.check_layer(cfg, inp, gpu)
     assert summary["routing_diff"] == 0 or summary["near_ties"] > 0
@@ -271,14 +278,16 @@ def _random_workloads(n=24, seed=2024):
         out.append(MoEWorkload(f"rand{i}", T=T, d=d, F=F, N=N, K=K, dtype=dtype, activation=act,
                                has_bias=bias, init=init, capacity_factor=cf,
                                add_residual=bool(rng.integers(0, 2)),
-                               router_bias=str(rng.choice(["none", "uniform"]))))
+                               router_bias=str(rng.choice(["none", "uniform"])),
+                               gate_mode=str(rng.choice(["renorm", "renorm", "softmax"])),
+                               select_bias=str(rng.choice(["none", "none", "uniform"]))))
     return out
 
 
 @pytest.mark.parametrize("w", _random_workloads(), ids=lambda w: w.name)
 def test_random_layers(w):
-    cfg = moe.LayerConfig.from_workload(w)
     inp = L.device_inputs(w)
+    cfg = L.layer_config(w, inp)
     gpu = L.run_stages(cfg, inp)
     L.check_layer(cfg, inp, gpu, bound="rounding")
     y_fwd, _ = L.run_forward(cfg, inp)
