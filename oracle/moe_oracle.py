@@ -19,7 +19,7 @@ is rounded on the way. Each function names the passage it follows. Sources:
   [概念卡]       "混合专家模型（Mixture of Experts, MoE）" (learnagent.wiki):
                  结构 2, 结构 3, 结构 4, 运行示例.
   [替代FFN]      "MoE 如何替代 FFN？它解决了什么问题？带来哪些新挑战？"
-                 (mstx.cn): §1, §2, §4 (6).
+                 (mstx.cn): §1, §2, §4 (6), §5.
 
 Readings where the pages are silent or disagree (each one is listed with its
 reason in the design notes):
@@ -36,7 +36,9 @@ reason in the design notes):
   * GELU is the exact-erf form;
   * router z-loss (no formula on the pages) is the mean over tokens of the
     squared log-sum-exp of the logits; the selection bias changes the top-K
-    choice only.
+    choice only;
+  * shared experts (named, not formulated, on the pages) take every token
+    with gate 1, bypass router and capacity and stay out of the statistics.
 
 Every function here is pinned by tests/test_oracle_pins.py against values
 the pages print, closed forms, special cases and brute force.
@@ -288,10 +290,23 @@ def stacked_expert(weights: dict, e: int) -> dict:
 # the layer: [稀疏激活原理] §三 MoELayer.forward; [概念卡] 核心原理 (four
 # steps) and 结构 3 (y = Σ_{i∈TopK} G(x)_i E_i(x))
 # --------------------------------------------------------------------------
+def shared_experts_output(xs: np.ndarray, expert_of, N: int, n_shared: int,
+                          activation: str) -> np.ndarray:
+    """[替代FFN] §5 (DeepSeek-MoE: fine-grained experts plus shared experts):
+    the shared experts N .. N+n_shared-1 run on every token with gate 1,
+    outside the router and the capacity, and their outputs add to the layer
+    output."""
+    out = np.zeros_like(xs)
+    for s in range(n_shared):
+        ew = {kk: f64(v) for kk, v in expert_of(N + s).items() if v is not None}
+        out = out + expert_apply(activation, xs, ew)
+    return out
+
+
 def moe_forward(x, w_r, b_r, expert_of, *, K: int, activation: str,
                 capacity_factor: float = math.inf, alpha: float = 0.01,
                 add_residual: bool = False, tokens=None, idx_override=None,
-                gate_mode: str = "renorm", select_bias=None):
+                gate_mode: str = "renorm", select_bias=None, n_shared: int = 0):
     """The whole layer in float64.
 
     expert_of(e) returns expert e's weights (dict of arrays, promoted here).
@@ -301,7 +316,8 @@ def moe_forward(x, w_r, b_r, expert_of, *, K: int, activation: str,
     GPU choice among near-tied logits); gates are recomputed from it.
     gate_mode: "renorm" (softmax over the K selected logits) or "softmax"
     (full-softmax probabilities, not renormalised). select_bias: [N] bias
-    for the top-K choice only.
+    for the top-K choice only. n_shared: shared experts (indices N.. of
+    expert_of) added to every token with gate 1.
     Returns a dict of every intermediate the layer defines."""
     xs = f64(x)
     T = xs.shape[0]
@@ -335,11 +351,15 @@ def moe_forward(x, w_r, b_r, expert_of, *, K: int, activation: str,
         oe = expert_apply(activation, xs[[t for (_, t, _) in rows]], ew)
         for r, (i, t, k) in enumerate(rows):
             o_of[(i, k)] = oe[r]
+    shared = (shared_experts_output(xs[tok], expert_of, N, n_shared, activation)
+              if n_shared > 0 and len(tok) > 0 else None)
     for i, t in enumerate(tok):
         acc = np.zeros(xs.shape[1])
         for k in range(K):
             if (i, k) in o_of:
                 acc = acc + gate[t, k] * o_of[(i, k)]
+        if shared is not None:
+            acc = acc + shared[i]
         y[i] = acc + (xs[t] if add_residual else 0.0)
     return {"logits": l, "p": p, "idx": idx, "gate": gate, "count": count, "f": f,
             "P": P, "l_aux": l_aux, "z_loss": router_z_loss(l), "entropy": routing_entropy(p),

@@ -513,3 +513,63 @@ def test_mutation_biased_gate_is_caught(monkeypatch):
     monkeypatch.setattr(O, "renormalised_gates", wrong)
     with pytest.raises(AssertionError):
         test_selection_bias_forces_expert_but_gate_uses_unbiased_logits()
+
+
+# ------------------------------------------------------ shared experts ----
+def _shared_layer(seed=31, T=12, d=8, F=10, N=4, S=2):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(size=(T, d))
+    w_r = rng.normal(size=(N, d))
+    W = {"w_gate": rng.normal(size=(N + S, F, d)) * 0.3, "w_up": rng.normal(size=(N + S, F, d)) * 0.3,
+         "w_down": rng.normal(size=(N + S, d, F)) * 0.3}
+    return x, w_r, W, (lambda e: O.stacked_expert(W, e))
+
+
+def test_shared_experts_add_plain_ffns():
+    """[替代FFN] §5 and §1: with shared experts the output gains, on every token,
+    each shared expert's FFN(x) = W_down (silu(W_gate x) * (W_up x))."""
+    x, w_r, W, ex = _shared_layer()
+    base = O.moe_forward(x, w_r, None, ex, K=2, activation="swiglu")
+    withs = O.moe_forward(x, w_r, None, ex, K=2, activation="swiglu", n_shared=2)
+    direct = sum(((torch.nn.functional.silu(torch.from_numpy(x @ W["w_gate"][4 + s].T))).numpy()
+                  * (x @ W["w_up"][4 + s].T)) @ W["w_down"][4 + s].T for s in range(2))
+    assert np.max(np.abs(withs["y"] - base["y"] - direct)) < 1e-12
+    # routing and statistics do not see the shared experts
+    for k in ("idx", "gate", "count", "P", "kept", "offsets"):
+        assert np.array_equal(base[k], withs[k])
+
+
+def test_shared_experts_survive_zero_capacity():
+    """Capacity drops only routed assignments: with C = 0 the output is the
+    shared experts' sum (plus x with the residual)."""
+    x, w_r, W, ex = _shared_layer(seed=32)
+    r = O.moe_forward(x, w_r, None, ex, K=2, activation="swiglu", capacity_factor=0.01,
+                      n_shared=2, add_residual=True)
+    assert r["C"] == 0
+    assert np.max(np.abs(r["y"] - x - O.shared_experts_output(x, ex, 4, 2, "swiglu"))) < 1e-12
+
+
+def test_shared_expert_equals_always_routed_expert():
+    """One shared expert is the same as an extra routed expert that every
+    token picks with gate 1: a 2-expert layer whose router always picks
+    expert 1 (K=1, renormalised gate = 1) over expert 0 equals a 1-expert
+    layer whose expert 0 never fires (capacity 0) plus expert 1 as shared."""
+    rng = np.random.default_rng(33)
+    x = rng.normal(size=(9, 6))
+    W = {"w_gate": rng.normal(size=(2, 7, 6)), "w_up": rng.normal(size=(2, 7, 6)),
+         "w_down": rng.normal(size=(2, 6, 7))}
+    ex = lambda e: O.stacked_expert(W, e)
+    w_r = np.zeros((2, 6))
+    b_r = np.array([0.0, 50.0])
+    routed = O.moe_forward(x, w_r, b_r, ex, K=1, activation="swiglu")
+    shared = O.moe_forward(x, np.zeros((1, 6)), None, ex, K=1, activation="swiglu",
+                           capacity_factor=0.01, n_shared=1)
+    assert np.max(np.abs(routed["y"] - shared["y"])) < 1e-12
+
+
+def test_mutation_shared_gate_is_caught(monkeypatch):
+    orig = O.shared_experts_output
+    monkeypatch.setattr(O, "shared_experts_output",
+                        lambda xs, ex, N, S, act: 0.5 * orig(xs, ex, N, S, act))
+    with pytest.raises(AssertionError):
+        test_shared_experts_add_plain_ffns()
