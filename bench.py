@@ -428,8 +428,9 @@ def run_ours(args, world, rank):
     st = layer.stats.to_host()
     if st["status"] != 0:
         raise SystemExit(f"device status word {st['status']:#x} after the timed steps")
-    kept = int(st["kept"].sum())
-    active = int((st["kept"] > 0).sum())
+    # shared experts process every token: T more rows each, always active
+    kept = int(st["kept"].sum()) + w.n_shared * w.T
+    active = int((st["kept"] > 0).sum()) + w.n_shared
     work = algorithmic_work(w, kept, active)
     peaks = measured_peaks()
     gu_s = statistics.mean(stage_ms["ffn_gate_up"]) / 1e3

@@ -16,8 +16,9 @@
  *   [替代FFN]      "MoE 如何替代 FFN？它解决了什么问题？带来哪些新挑战？"
  *                  (mstx.cn/posts/467.html): §1 标准 FFN, §2 MoE 如何替代 FFN.
  *
- * Notation: T tokens, d = d_model, N experts, K = top-K, F = d_ff,
- * C = per-expert capacity, A = number of kept (token, rank) assignments.
+ * Notation: T tokens, d = d_model, N routed experts, S shared experts,
+ * K = top-K, F = d_ff, C = per-expert capacity, A = number of kept
+ * (token, rank) assignments, R_max = A_max + S*T rows of permuted tokens.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -37,9 +38,9 @@
  *    when stats and stats->status are non-NULL; read it after a sync.
  *    The caller zeroes *status before the call if it wants a fresh word.
  *    No C++ exception crosses this ABI.
- *  - Limits: 1 <= K <= min(N, 8); N <= 256; 1 <= T <= 2^24 (T = 0 is
- *    accepted and does nothing); d % 8 == 0 for bf16, d % 4 == 0 for fp32;
- *    F % 4 == 0.
+ *  - Limits: 1 <= K <= min(N, 8); N <= 256; 0 <= S <= 8; 1 <= T <= 2^24
+ *    (T = 0 is accepted and does nothing); d % 8 == 0 for bf16, d % 4 == 0
+ *    for fp32; F % 4 == 0.
  *  - Determinism: every result is bitwise reproducible run to run (fixed
  *    reduction orders, no floating-point atomics).
  */
@@ -97,6 +98,10 @@ typedef struct {
                            the top-K choice only; gates and statistics use the
                            unbiased logits (auxiliary-loss-free balancing,
                            [概念卡] 结构 4)                                    */
+  int32_t n_shared;   /* S in [0, 8]: shared experts, stacked after the N
+                           routed ones in every weight array; each takes every
+                           token with gate 1, outside the router, the capacity
+                           and the statistics ([替代FFN] §5, DeepSeek-MoE)     */
 } moe_config;
 
 /* Device-side statistics; every member is a caller-owned DEVICE pointer and
@@ -126,10 +131,11 @@ typedef struct {
 } moe_stats;
 
 /* Expert weights, stacked over experts, in the nn.Linear (out, in) layout of
- * each expert ([稀疏激活原理] §三 class Expert; [概念卡] 运行示例).
+ * each expert ([稀疏激活原理] §三 class Expert; [概念卡] 运行示例): the N
+ * routed experts, then the S shared ones (E = N + S).
  * Element type is cfg->dtype. Unused members are NULL.
- *   SwiGLU: w_gate [N][F][d], w_up [N][F][d], w_down [N][d][F]
- *   GELU:   w1 [N][F][d], w2 [N][d][F]; biases b1 [N][F], b2 [N][d]
+ *   SwiGLU: w_gate [E][F][d], w_up [E][F][d], w_down [E][d][F]
+ *   GELU:   w1 [E][F][d], w2 [E][d][F]; biases b1 [E][F], b2 [E][d]
  *           (same dtype), required iff cfg->has_bias.                      */
 typedef struct {
   const void* w_gate;
@@ -143,8 +149,8 @@ typedef struct {
 
 /* Bytes of workspace that moe_forward needs for cfg (an upper bound for the
  * other entry points too). Pure host function; returns 0 if cfg is invalid.
- * It covers x_perm [A_max][d], h [A_max][F] and o [A_max][d] fp32, where
- * A_max = min(T*K, N*C). */
+ * It covers x_perm [R_max][d], h [R_max][F] and o [R_max][d] fp32, where
+ * A_max = min(T*K, N*C) and R_max = A_max + S*T. */
 size_t moe_workspace_size(const moe_config* cfg);
 
 /* Capacity C per expert: floor(K * CF * T / N), computed exactly on the
@@ -202,12 +208,15 @@ moe_status moe_route_no_workspace(const moe_config* cfg, const void* x,
  * contiguous slots [offsets[e], offsets[e+1]) in that visiting order, and
  * x_perm[slot] = x[t]. Dropped assignments get slot_of = -1 and contribute
  * nothing to y (the residual carries the token, [稀疏激活原理] §2.3).
+ * Shared expert s (index N + s) takes every token in order: its slots are
+ * offsets[N+s] + t with offsets[N+s] = offsets[N] + s*T, recorded as
+ * slot_of[t][K+s].
  * [稀疏激活原理] §2.3 and §三 MoELayer.forward (outer loop over top-k rank,
  * tokens in ascending order, truncation at capacity).
  *   x [T][d] cfg->dtype, idx [T][K] int32 (values in [0, N))
- *   offsets [N+1] int32 (out), slot_of [T][K] int32 (out),
- *   token_of_slot [A_max] int32 (out, first offsets[N] valid),
- *   x_perm [A_max][d] cfg->dtype (out).
+ *   offsets [N+S+1] int32 (out), slot_of [T][K+S] int32 (out),
+ *   token_of_slot [R_max] int32 (out, first offsets[N] valid),
+ *   x_perm [R_max][d] cfg->dtype (out).
  *   stats: count, kept, n_dropped, status are written.
  * Errors: as moe_route; device: MOE_ERR_INDEX (bad idx value; that
  * assignment is treated as dropped). */
@@ -216,8 +225,8 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x,
                         int32_t* token_of_slot, void* x_perm, moe_stats* stats,
                         void* ws, moe_stream_t stream);
 
-/* Grouped expert FFN over the permuted tokens: for every expert e and every
- * slot s in [offsets[e], offsets[e+1]),
+/* Grouped expert FFN over the permuted tokens: for every expert e < N + S
+ * and every slot s in [offsets[e], offsets[e+1]),
  *   SwiGLU: o[s] = W_down,e (silu(W_gate,e x) * (W_up,e x))
  *   GELU:   o[s] = W2,e gelu_erf(W1,e x + b1,e) + b2,e
  * with x = x_perm[s]; silu(a) = a / (1 + e^-a); gelu_erf(z) =
@@ -225,8 +234,9 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x,
  * (bf16 or fp32) before the down projection; o is fp32.
  * [稀疏激活原理] §三 class Expert (SwiGLU); [概念卡] 运行示例
  * (Linear -> GELU -> Linear); [替代FFN] §1 (FFN(x) = W_2 act(W_1 x)).
- *   x_perm [A_max][d] cfg->dtype, offsets [N+1] int32 (device, as written by
- *   moe_dispatch), o [A_max][d] fp32 (out). Rows past offsets[N] untouched.
+ *   x_perm [R_max][d] cfg->dtype, offsets [N+S+1] int32 (device, as written
+ *   by moe_dispatch), o [R_max][d] fp32 (out). Rows past offsets[N+S]
+ *   untouched.
  * Errors: as moe_route; device: MOE_ERR_TIMEOUT. */
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm,
                           const int32_t* offsets,
@@ -234,11 +244,12 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm,
                           moe_stats* stats, void* ws, moe_stream_t stream);
 
 /* Gate-weighted combine: y[t] = sum over k ascending with slot_of[t][k] >= 0
- * of gate[t][k] * o[slot_of[t][k]], accumulated in fp32 and rounded once to
- * cfg->dtype; plus x[t] when cfg->add_residual. No atomics.
+ * of gate[t][k] * o[slot_of[t][k]], then + o[slot_of[t][K+s]] for the
+ * shared experts s ascending (gate 1), accumulated in fp32 and rounded once
+ * to cfg->dtype; plus x[t] when cfg->add_residual. No atomics.
  * [概念卡] 结构 3 (y = Σ_{i∈TopK} G(x)_i E_i(x)); [替代FFN] §2 (MoE(x) formula);
  * [稀疏激活原理] §2.1.
- *   o [A_max][d] fp32, slot_of [T][K] int32, gate [T][K] fp32,
+ *   o [R_max][d] fp32, slot_of [T][K+S] int32, gate [T][K] fp32,
  *   x [T][d] (read only if add_residual; may be NULL otherwise),
  *   y [T][d] cfg->dtype (out).
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */

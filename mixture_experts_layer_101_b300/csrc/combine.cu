@@ -1,4 +1,5 @@
-// Gate-weighted combine: y[t] = sum_k gate[t][k] * o[slot_of[t][k]] (+ x[t]).
+// Gate-weighted combine: y[t] = sum_k gate[t][k] * o[slot_of[t][k]]
+// + sum_s o[slot_of[t][K+s]] (shared experts, gate 1) (+ x[t]).
 //
 // Sources: "混合专家模型（Mixture of Experts, MoE）" 结构 3 (y = Σ_{i∈TopK}
 // G(x)_i·E_i(x)); "MoE 如何替代 FFN？…" §2 (MoE(x) = Σ g(x)_i·Expert_i(x));
@@ -20,18 +21,20 @@ template <typename Tx>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_of,
                const float* __restrict__ gate, const Tx* __restrict__ x, Tx* __restrict__ y,
-               int K, int d, int add_residual) {
-  __shared__ int32_t s_slot[8];
-  __shared__ float s_gate[8];
+               int K, int S, int d, int add_residual) {
+  __shared__ int32_t s_slot[16];
+  __shared__ float s_gate[16];
   const int t = blockIdx.x;
-  if (threadIdx.x < K) {
-    s_slot[threadIdx.x] = slot_of[static_cast<size_t>(t) * K + threadIdx.x];
-    s_gate[threadIdx.x] = gate[static_cast<size_t>(t) * K + threadIdx.x];
+  const int KS = K + S;  // routed ranks, then shared experts with gate 1
+  if (threadIdx.x < KS) {
+    s_slot[threadIdx.x] = slot_of[static_cast<size_t>(t) * KS + threadIdx.x];
+    s_gate[threadIdx.x] =
+        threadIdx.x < K ? gate[static_cast<size_t>(t) * K + threadIdx.x] : 1.f;
   }
   __syncthreads();
   for (int c = threadIdx.x * 4; c < d; c += kThreads * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < K; ++k) {
+    for (int k = 0; k < KS; ++k) {
       const int s = s_slot[k];
       if (s < 0) continue;
       const float g = s_gate[k];
@@ -60,11 +63,11 @@ moe_status launch_combine(const moe_config& c, const float* o, const int32_t* sl
   if (c.dtype == MOE_BF16)
     combine_kernel<__nv_bfloat16><<<c.T, kThreads, 0, s>>>(
         o, slot_of, gate, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y),
-        c.top_k, c.d_model, c.add_residual);
+        c.top_k, c.n_shared, c.d_model, c.add_residual);
   else
     combine_kernel<float><<<c.T, kThreads, 0, s>>>(o, slot_of, gate, static_cast<const float*>(x),
-                                                   static_cast<float*>(y), c.top_k, c.d_model,
-                                                   c.add_residual);
+                                                   static_cast<float*>(y), c.top_k, c.n_shared,
+                                                   c.d_model, c.add_residual);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -13,6 +13,9 @@
 // + assignments to e in earlier warps of this block
 // + earlier lanes of this warp with the same expert (warp match).
 // Every step is integer and order-defined, so slots are bit-exact.
+// Shared experts (indices N .. N+S-1) follow the routed slots: shared expert
+// s takes every token in order, slots offsets[N] + s*T + t, recorded in
+// slot_of[t][K+s].
 #include "moe_common.cuh"
 
 namespace moe {
@@ -41,7 +44,7 @@ dispatch_hist_kernel(const int32_t* __restrict__ idx, int T, int K, int N,
 // One block. Thread e scans its expert's column over the K*nb (k, b) blocks
 // in visiting order; then the kept counts are scanned over experts.
 __global__ void __launch_bounds__(256)
-dispatch_scan_kernel(const int32_t* __restrict__ ghist, int nq, int N, int32_t C,
+dispatch_scan_kernel(const int32_t* __restrict__ ghist, int nq, int N, int32_t C, int S, int T,
                      int32_t* __restrict__ gbase, int32_t* __restrict__ offsets,
                      int32_t* count, int32_t* kept_out, int32_t* n_dropped) {
   __shared__ int32_t kept[256], cnt[256];
@@ -65,12 +68,13 @@ dispatch_scan_kernel(const int32_t* __restrict__ ghist, int nq, int N, int32_t C
       dropped += cnt[e] - kept[e];
     }
     offsets[N] = off;
+    for (int s = 0; s < S; ++s) offsets[N + s + 1] = off + (s + 1) * T;  // shared experts
     if (n_dropped) *n_dropped = dropped;
   }
 }
 
 __global__ void __launch_bounds__(kThreads)
-dispatch_permute_kernel(const int32_t* __restrict__ idx, int T, int K, int N, int32_t C,
+dispatch_permute_kernel(const int32_t* __restrict__ idx, int T, int K, int N, int S, int32_t C,
                         const int32_t* __restrict__ gbase, const int32_t* __restrict__ offsets,
                         int32_t* __restrict__ slot_of, int32_t* __restrict__ token_of_slot) {
   __shared__ int32_t wcnt[kThreads / 32][256];
@@ -91,6 +95,7 @@ dispatch_permute_kernel(const int32_t* __restrict__ idx, int T, int K, int N, in
   if (valid && rank_w == 0) wcnt[warp][e] = __popc(peers);
   __syncthreads();
 
+  const int KS = K + S;  // slot_of row: K routed ranks, then the shared experts
   int32_t slot = -1;
   if (valid) {
     int32_t rank = gbase[(static_cast<size_t>(k) * nb + b) * N + e] + rank_w;
@@ -100,7 +105,12 @@ dispatch_permute_kernel(const int32_t* __restrict__ idx, int T, int K, int N, in
       token_of_slot[slot] = t;
     }
   }
-  if (t < T) slot_of[static_cast<size_t>(t) * K + k] = slot;
+  if (t < T) {
+    slot_of[static_cast<size_t>(t) * KS + k] = slot;
+    if (k == 0)
+      for (int s2 = 0; s2 < S; ++s2)
+        slot_of[static_cast<size_t>(t) * KS + K + s2] = offsets[N] + s2 * T + t;
+  }
 }
 
 // x_perm[s] = x[token_of_slot[s]] for s < offsets[N]: one warp per slot, 16
@@ -108,12 +118,14 @@ dispatch_permute_kernel(const int32_t* __restrict__ idx, int T, int K, int N, in
 template <typename Tx>
 __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ token_of_slot,
-                       const int32_t* __restrict__ offsets, int N, int d, Tx* __restrict__ x_perm) {
-  const int total = offsets[N];
+                       const int32_t* __restrict__ offsets, int N, int S, int T, int d,
+                       Tx* __restrict__ x_perm) {
+  const int routed = offsets[N];
   const int slot = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (slot >= total) return;
+  if (slot >= routed + S * T) return;
   const int lane = threadIdx.x & 31;
-  const int t = token_of_slot[slot];
+  // routed slots come from the permutation; shared slots hold the tokens in order
+  const int t = slot < routed ? token_of_slot[slot] : (slot - routed) % T;
   const int chunks = d * static_cast<int>(sizeof(Tx)) / 16;
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
   uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(slot) * d);
@@ -143,24 +155,25 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
     dispatch_hist_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, ghist, status);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(ghist, c.T > 0 ? K * nb : 0, N, C, gbase, offsets,
+  dispatch_scan_kernel<<<1, 256, 0, s>>>(ghist, c.T > 0 ? K * nb : 0, N, C, c.n_shared, c.T,
+                                         gbase, offsets,
                                          st ? st->count : nullptr, st ? st->kept : nullptr,
                                          st ? st->n_dropped : nullptr);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   if (c.T > 0) {
-    dispatch_permute_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, C, gbase, offsets,
-                                                             slot_of, token_of_slot);
+    dispatch_permute_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, c.n_shared, C, gbase,
+                                                             offsets, slot_of, token_of_slot);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-    const int64_t a_max = a_max_of(&c);
-    const unsigned gblocks = static_cast<unsigned>((a_max + 7) / 8);
+    const int64_t rows = rows_max_of(&c);
+    const unsigned gblocks = static_cast<unsigned>((rows + 7) / 8);
     if (gblocks > 0) {
       if (c.dtype == MOE_BF16)
         dispatch_gather_kernel<__nv_bfloat16><<<gblocks, 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(x), token_of_slot, offsets, N, c.d_model,
-            static_cast<__nv_bfloat16*>(x_perm));
+            static_cast<const __nv_bfloat16*>(x), token_of_slot, offsets, N, c.n_shared, c.T,
+            c.d_model, static_cast<__nv_bfloat16*>(x_perm));
       else
         dispatch_gather_kernel<float><<<gblocks, 256, 0, s>>>(
-            static_cast<const float*>(x), token_of_slot, offsets, N, c.d_model,
+            static_cast<const float*>(x), token_of_slot, offsets, N, c.n_shared, c.T, c.d_model,
             static_cast<float*>(x_perm));
       if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }

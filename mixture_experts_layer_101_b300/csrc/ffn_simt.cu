@@ -120,7 +120,7 @@ grouped_gemm_simt(const T* __restrict__ A, const T* __restrict__ B0, const T* __
 template <typename T>
 moe_status run(const moe_config& c, int64_t a_max, const T* x_perm, const int32_t* offsets,
                const moe_expert_weights& w, T* h, float* o, cudaStream_t s, int part) {
-  const int N = c.n_experts, d = c.d_model, F = c.d_ff;
+  const int N = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
   const int64_t mtiles = N + (a_max + BM - 1) / BM;  // upper bound on (expert, m-tile) pairs
   if (mtiles > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
   dim3 g1(static_cast<unsigned>(mtiles), (F + BN - 1) / BN), g2(static_cast<unsigned>(mtiles),

@@ -44,7 +44,7 @@ namespace {
 constexpr int BM = 128, BK = 64, kThreads = 192;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
 constexpr int ACC_COLS = 256;           // fp32 accumulator 128 x 256 (CTA-pair kernel)
-constexpr int MAX_EXPERTS = 256;
+constexpr int MAX_EXPERTS = 264;  // 256 routed + 8 shared
 
 // Tile shape of the one-CTA kernel. MODE 0 (gate/up): BNH output columns of
 // h per tile, i.e. BNH gate rows + BNH up rows of weights, MMA N = 2*BNH.
@@ -131,8 +131,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tmem_relinquish();
   }
   if (warp == 2) {
-    // tile_start[e] = tiles of experts < e; lane owns experts [8*lane, 8*lane+8)
-    constexpr int PER = MAX_EXPERTS / 32;
+    // tile_start[e] = tiles of experts < e; lane owns experts [PER*lane, PER*lane+PER)
+    constexpr int PER = (MAX_EXPERTS + 31) / 32;
     int local[PER], sum = 0;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
@@ -427,7 +427,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
     tmem_relinquish_pair();
   }
   if (warp == 2) {
-    constexpr int PER = MAX_EXPERTS / 32;
+    constexpr int PER = (MAX_EXPERTS + 31) / 32;
     int local[PER], sum = 0;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
@@ -705,8 +705,8 @@ bool set_smem_attr() {
 // CTA pairs pay off when experts have several 128-row tiles (then both CTAs
 // of a pair compute stored rows); with about one tile per expert the odd CTA
 // would mostly compute discarded rows.
-bool use_pairs(const moe_config& c, int64_t a_max) {
-  return a_max >= static_cast<int64_t>(c.n_experts) * BM * 4;
+bool use_pairs(const moe_config& c, int64_t rows) {
+  return rows >= static_cast<int64_t>(c.n_experts + c.n_shared) * BM * 4;
 }
 
 template <int MODE>
@@ -734,14 +734,14 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 
 bool ffn_tc_supported(const moe_config& c) {
   return c.dtype == MOE_BF16 && c.activation == MOE_SWIGLU && c.d_model % 256 == 0 &&
-         c.d_ff % 128 == 0 && c.n_experts <= MAX_EXPERTS;
+         c.d_ff % 128 == 0 && c.n_experts + c.n_shared <= MAX_EXPERTS;
 }
 
 moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w, void* h, float* o,
                          uint32_t* status, cudaStream_t s, int part) {
   if (a_max == 0) return MOE_OK;
-  const int N = c.n_experts, d = c.d_model, F = c.d_ff;
+  const int N = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
   const bool pairs = use_pairs(c, a_max);
   CUtensorMap mx, mg, mu, mh, md;
   if (!make_map(&mx, x_perm, a_max, d, 128) ||

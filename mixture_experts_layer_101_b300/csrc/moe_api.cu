@@ -31,6 +31,8 @@ bool config_valid(const moe_config* c, moe_status* why) {
     return bad(MOE_ERR_INVALID);
   if (c->gate_mode != MOE_GATE_RENORM && c->gate_mode != MOE_GATE_SOFTMAX)
     return bad(MOE_ERR_INVALID);
+  if (c->n_shared < 0) return bad(MOE_ERR_INVALID);
+  if (c->n_shared > 8) return bad(MOE_ERR_UNSUPPORTED);
   if (c->T < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0)
     return bad(MOE_ERR_INVALID);
   if (c->top_k > c->n_experts) return bad(MOE_ERR_INVALID);
@@ -62,6 +64,10 @@ int64_t a_max_of(const moe_config* c) {
   return tk < nc ? tk : nc;
 }
 
+int64_t rows_max_of(const moe_config* c) {
+  return a_max_of(c) + static_cast<int64_t>(c->n_shared) * c->T;
+}
+
 WsLayout ws_layout(const moe_config* c) {
   WsLayout L{};
   size_t total = 0;
@@ -76,7 +82,8 @@ WsLayout ws_layout(const moe_config* c) {
   L.nblk_r = static_cast<int>((T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock);
   L.nblk_d = static_cast<int>((T + kDispatchTokensPerBlock - 1) / kDispatchTokensPerBlock);
   const size_t nr = L.nblk_r > 0 ? L.nblk_r : 1, nd = L.nblk_d > 0 ? L.nblk_d : 1;
-  const size_t A = static_cast<size_t>(L.a_max);
+  const size_t A = static_cast<size_t>(rows_max_of(c));  // routed + shared rows
+  const size_t S = static_cast<size_t>(c->n_shared);
   L.idx = take(T * K * 4);
   L.gate = take(T * K * 4);
   L.psum = take(nr * (N + 2) * 4);  // rows N, N+1: z-loss and entropy partials
@@ -86,8 +93,8 @@ WsLayout ws_layout(const moe_config* c) {
   L.part = take(rp.use ? static_cast<size_t>(rp.S) * T * rp.NP * 4 : 0);
   L.ghist = take(K * nd * N * 4);
   L.gbase = take(K * nd * N * 4);
-  L.offsets = take((N + 1) * 4);
-  L.slot_of = take(T * K * 4);
+  L.offsets = take((N + S + 1) * 4);
+  L.slot_of = take(T * (K + S) * 4);
   L.token_of_slot = take((A > 0 ? A : 1) * 4);
   L.x_perm = take(A * d * es);
   L.h = take(A * F * es);
@@ -160,8 +167,9 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
   const bool tc = ffn_tc_supported(*c);
   uint32_t* status = stats ? stats->status : nullptr;
   for (int part = 1; part <= 2; ++part) {
-    const moe_status r = tc ? launch_ffn_tc(*c, L.a_max, x_perm, offsets, *w, h, o, status, s, part)
-                            : launch_ffn_simt(*c, L.a_max, x_perm, offsets, *w, h, o, s, part);
+    const int64_t rows = rows_max_of(c);
+    const moe_status r = tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, status, s, part)
+                            : launch_ffn_simt(*c, rows, x_perm, offsets, *w, h, o, s, part);
     if (r != MOE_OK) return r;
     if (traced) trace(2 + part, s);
   }

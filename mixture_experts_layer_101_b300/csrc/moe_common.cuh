@@ -74,6 +74,7 @@ struct WsLayout {
 bool config_valid(const moe_config* c, moe_status* why);
 int32_t capacity_of(const moe_config* c);
 int64_t a_max_of(const moe_config* c);
+int64_t rows_max_of(const moe_config* c);  // routed A_max + n_shared * T
 WsLayout ws_layout(const moe_config* c);
 int sm_count();
 
@@ -110,15 +111,16 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
 moe_status launch_combine(const moe_config& c, const float* o, const int32_t* slot_of,
                           const float* gate, const void* x, void* y, cudaStream_t s);
 
-// Expert FFN on CUDA cores (any dtype/shape). part: 1 = gate/up (or the
-// first Linear + GELU) into h, 2 = down projection into o, 3 = both.
-moe_status launch_ffn_simt(const moe_config& c, int64_t a_max, const void* x_perm,
+// Expert FFN on CUDA cores (any dtype/shape) over the N + n_shared experts;
+// rows = rows of x_perm / h / o. part: 1 = gate/up (or the first Linear +
+// GELU) into h, 2 = down projection into o, 3 = both.
+moe_status launch_ffn_simt(const moe_config& c, int64_t rows, const void* x_perm,
                            const int32_t* offsets, const moe_expert_weights& w,
                            void* h, float* o, cudaStream_t s, int part);
 
 // Expert FFN on tcgen05 tensor cores (bf16, d % 256 == 0, F % 128 == 0).
 bool ffn_tc_supported(const moe_config& c);
-moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
+moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w,
                          void* h, float* o, uint32_t* status, cudaStream_t s, int part);
 

@@ -45,7 +45,8 @@ class MoEConfig(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("activation", ctypes.c_int32),
                 ("has_bias", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
                 ("alpha", ctypes.c_float), ("add_residual", ctypes.c_int32),
-                ("gate_mode", ctypes.c_int32), ("select_bias", ctypes.c_void_p)]
+                ("gate_mode", ctypes.c_int32), ("select_bias", ctypes.c_void_p),
+                ("n_shared", ctypes.c_int32)]
 
 
 class MoEStatsC(ctypes.Structure):
@@ -129,13 +130,15 @@ class LayerConfig:
     add_residual: bool = False
     gate_mode: str = "renorm"          # "renorm" | "softmax"
     select_bias: torch.Tensor | None = None  # [N] fp32 CUDA tensor: top-K choice only
+    n_shared: int = 0                  # shared experts after the N routed ones
 
     @classmethod
     def from_workload(cls, w, T: int | None = None) -> "LayerConfig":
         return cls(T=w.T if T is None else T, d_model=w.d, d_ff=w.F, n_experts=w.N, top_k=w.K,
                    dtype=w.dtype, activation=w.activation, has_bias=w.has_bias,
                    capacity_factor=w.capacity_factor, alpha=w.alpha, add_residual=w.add_residual,
-                   gate_mode=getattr(w, "gate_mode", "renorm"))
+                   gate_mode=getattr(w, "gate_mode", "renorm"),
+                   n_shared=getattr(w, "n_shared", 0))
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -148,7 +151,7 @@ class LayerConfig:
                          int(self.has_bias), float(self.capacity_factor), float(self.alpha),
                          int(self.add_residual),
                          MOE_GATE_SOFTMAX if self.gate_mode == "softmax" else MOE_GATE_RENORM,
-                         _ptr(self.select_bias))
+                         _ptr(self.select_bias), int(self.n_shared))
 
 
 def _ptr(t) -> int | None:
@@ -241,8 +244,14 @@ moe_forward_launch_count = forward_launch_count
 
 
 def a_max(cfg: LayerConfig) -> int:
+    """Most routed assignments capacity lets through: min(T*K, N*C)."""
     C = capacity(cfg)
     return min(cfg.T * cfg.top_k, cfg.n_experts * C)
+
+
+def rows_max(cfg: LayerConfig) -> int:
+    """Rows of the permuted buffers (x_perm, h, o): routed A_max + shared S*T."""
+    return a_max(cfg) + cfg.n_shared * cfg.T
 
 
 def alloc_workspace(cfg: LayerConfig, device="cuda") -> torch.Tensor:

@@ -14,6 +14,8 @@ Workloads (shapes and distributions of the layers the MoE pages discuss):
   mixtral_decode   T=16, same weights and shapes as mixtral_prefill.
   deepseek_fine    T=4096, d=7168, N=256, K=8, SwiGLU F=2048, router
                    7168->256 fp32; x ~ N(0,1); weights ~ N(0, 0.02).
+  deepseek_shared  deepseek_fine plus one shared expert (F=2048) on every
+                   token (the fine-grained + shared layout of DeepSeek-MoE).
   switch_skewed    T=32768 (16x2048), d=1024, N=64, K=1, SwiGLU F=4096,
                    CF=1.25 (capacity 640), residual on; router bias
                    SWITCH_SKEW_BIAS on experts 0..3 so that about 70% of the
@@ -67,6 +69,7 @@ class MoEWorkload:
     router_std: float = 0.02
     gate_mode: str = "renorm"    # "renorm" | "softmax"
     select_bias: str = "none"    # "none" | "uniform": a top-K selection bias
+    n_shared: int = 0            # shared experts, seeds 1 + N + s after the routed ones
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -80,6 +83,8 @@ WORKLOADS = {
     "mixtral_prefill": MoEWorkload("mixtral_prefill", T=4096, d=4096, F=14336, N=8, K=2),
     "mixtral_decode": MoEWorkload("mixtral_decode", T=16, d=4096, F=14336, N=8, K=2),
     "deepseek_fine": MoEWorkload("deepseek_fine", T=4096, d=7168, F=2048, N=256, K=8),
+    "deepseek_shared": MoEWorkload("deepseek_shared", T=4096, d=7168, F=2048, N=256, K=8,
+                                   n_shared=1),
     "switch_skewed": MoEWorkload("switch_skewed", T=32768, d=1024, F=4096, N=64, K=1,
                                  router_bias="skew", capacity_factor=1.25,
                                  add_residual=True),
@@ -171,13 +176,15 @@ def make_expert(w: MoEWorkload, e: int, device="cpu") -> dict:
 
 
 def make_experts(w: MoEWorkload, device="cpu") -> dict:
-    """All expert weights stacked over experts: [N][...] in the storage dtype."""
+    """All expert weights stacked over experts, the N routed ones then the
+    n_shared shared ones: [N + n_shared][...] in the storage dtype."""
     names = (["w_gate", "w_up", "w_down"] if w.activation == "swiglu"
              else (["w1", "b1", "w2", "b2"] if w.has_bias else ["w1", "w2"]))
     first = make_expert(w, 0, device)
-    stacked = {k: torch.empty((w.N,) + tuple(first[k].shape), dtype=first[k].dtype,
+    E = w.N + w.n_shared
+    stacked = {k: torch.empty((E,) + tuple(first[k].shape), dtype=first[k].dtype,
                               device=device) for k in names}
-    for e in range(w.N):
+    for e in range(E):
         ex = first if e == 0 else make_expert(w, e, device)
         for k in names:
             stacked[k][e].copy_(ex[k])

@@ -10,9 +10,9 @@ Comparison rules:
   * counts, kept, offsets, slots, token order and the drop set: bit-exact;
   * gates: |err| <= 1e-5; P and L_aux: relative error <= 1e-5;
   * y: max |err| <= 1e-4 * rms(y) for fp32 layers, <= 2e-2 * rms(y) for bf16
-    (the bars of the five named workloads); for random bf16 layers, where K=1
-    or small outputs leave nothing to average the bf16 roundings of h and y,
-    each element must lie within the bound those roundings allow
+    (the bars of the named workloads); for the small and random bf16 layers,
+    where K=1 or small outputs leave nothing to average the bf16 roundings of
+    h and y, each element must lie within the bound those roundings allow
     (bf16_rounding_bound).
 """
 from __future__ import annotations
@@ -58,14 +58,15 @@ def run_stages(cfg: moe.LayerConfig, inp: dict) -> dict:
     """route -> dispatch -> expert_ffn -> combine through the C ABI."""
     dev = "cuda"
     T, K, N, d = cfg.T, cfg.top_k, cfg.n_experts, cfg.d_model
-    A = moe.a_max(cfg)
+    S = cfg.n_shared
+    A = moe.rows_max(cfg)
     ws = moe.alloc_workspace(cfg)
     st = moe.Stats(N)
     idx = torch.full((T, K), -7, dtype=torch.int32, device=dev)
     gate = torch.zeros((T, K), dtype=torch.float32, device=dev)
     moe.moe_route(cfg, inp["x"], inp["w_r"], inp["b_r"], idx, gate, st, ws)
-    offsets = torch.zeros(N + 1, dtype=torch.int32, device=dev)
-    slot_of = torch.full((T, K), -7, dtype=torch.int32, device=dev)
+    offsets = torch.zeros(N + S + 1, dtype=torch.int32, device=dev)
+    slot_of = torch.full((T, K + S), -7, dtype=torch.int32, device=dev)
     tos = torch.full((max(A, 1),), -7, dtype=torch.int32, device=dev)
     x_perm = torch.zeros((max(A, 1), d), dtype=cfg.torch_dtype, device=dev)
     moe.moe_dispatch(cfg, inp["x"], idx, offsets, slot_of, tos, x_perm, st, ws)
@@ -116,6 +117,9 @@ def bf16_rounding_bound(cfg: moe.LayerConfig, inp: dict, ref: dict) -> np.ndarra
         for k in range(cfg.top_k):
             if ref["slot_of"][t, k] >= 0:
                 rows.setdefault(int(ref["idx"][t, k]), []).append((i, int(t), k))
+    for s in range(cfg.n_shared):  # shared experts: every token, gate 1
+        for i, t in enumerate(tok):
+            rows.setdefault(cfg.n_experts + s, []).append((i, int(t), -1))
     for e, lst in rows.items():
         ew = {kk: O.f64(v) for kk, v in reader(e).items() if v is not None}
         xe = x[[t for (_, t, _) in lst]]
@@ -128,7 +132,7 @@ def bf16_rounding_bound(cfg: moe.LayerConfig, inp: dict, ref: dict) -> np.ndarra
             wd = ew["w2"]
         scale = np.abs(h) @ np.abs(wd).T * 2.0 ** -9
         for r, (i, t, k) in enumerate(lst):
-            bound[i] += ref["gate"][t, k] * scale[r]
+            bound[i] += (ref["gate"][t, k] if k >= 0 else 1.0) * scale[r]
     y = ref["y"]
     rms = float(np.sqrt(np.mean(y ** 2))) if y.size else 0.0
     return bound + 2.0 ** -8 * np.abs(y) + 1e-3 * rms
@@ -149,7 +153,8 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
     ref = O.moe_forward(x, w_r, b_r, expert_reader(inp["experts"]), K=K,
                         activation=cfg.activation, capacity_factor=cfg.capacity_factor,
                         alpha=cfg.alpha, add_residual=cfg.add_residual, tokens=tokens,
-                        idx_override=idx_gpu, gate_mode=cfg.gate_mode, select_bias=sb)
+                        idx_override=idx_gpu, gate_mode=cfg.gate_mode, select_bias=sb,
+                        n_shared=cfg.n_shared)
     # gates and statistics
     assert np.max(np.abs(gpu["gate"].numpy() - ref["gate"]), initial=0) <= GATE_TOL
     st = gpu["stats"]
@@ -163,13 +168,20 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
     # dispatch: bit-exact
     assert np.array_equal(st["kept"], ref["kept"])
     assert st["n_dropped"] == ref["n_dropped"]
-    assert np.array_equal(gpu["offsets"].numpy(), ref["offsets"])
-    assert np.array_equal(gpu["slot_of"].numpy(), ref["slot_of"])
+    S, T = cfg.n_shared, cfg.T
+    offs = gpu["offsets"].numpy()
+    assert np.array_equal(offs[:N + 1], ref["offsets"])
     A = int(ref["offsets"][-1])
+    assert np.array_equal(offs[N:], A + T * np.arange(S + 1))   # shared experts: T rows each
+    assert np.array_equal(gpu["slot_of"].numpy()[:, :K], ref["slot_of"])
+    for s in range(S):
+        assert np.array_equal(gpu["slot_of"].numpy()[:, K + s], A + s * T + np.arange(T))
     assert np.array_equal(gpu["token_of_slot"].numpy()[:A], ref["token_of_slot"])
     if A > 0:
         tos = torch.from_numpy(ref["token_of_slot"])
         assert torch.equal(gpu["x_perm"][:A], inp["x"].cpu()[tos])
+    for s in range(S):
+        assert torch.equal(gpu["x_perm"][A + s * T:A + (s + 1) * T], inp["x"].cpu())
     # outputs
     tok = ref["tokens"]
     y_gpu = gpu["y"].double().numpy()[tok]

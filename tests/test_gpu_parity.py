@@ -53,6 +53,13 @@ SMALL = {
                                   capacity_factor=1.25, add_residual=True),
     "simt_softmax_bias_fp32": wl(T=100, d=36, F=52, N=6, K=3, dtype="f32", init="uniform",
                                  gate_mode="softmax", select_bias="uniform"),
+    # shared experts: every token, gate 1, outside capacity
+    "tc_shared_one": wl(T=300, d=256, F=256, N=8, K=2, n_shared=1),
+    "tc_shared_two_capacity": wl(T=600, d=512, F=128, N=16, K=2, n_shared=2,
+                                 capacity_factor=0.5, add_residual=True),
+    "tc_shared_pairs": wl(T=2048, d=256, F=256, N=2, K=1, n_shared=1),
+    "simt_shared_gelu_fp32": wl(T=90, d=64, F=96, N=4, K=2, n_shared=2, dtype="f32",
+                                activation="gelu", has_bias=True, init="uniform"),
     # CUDA-core path: fp32, GELU, or shapes the tensor-core kernel does not tile
     "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
     "simt_gelu_nobias": wl(T=90, d=64, F=96, N=4, K=2, dtype="f32", activation="gelu",
@@ -71,7 +78,7 @@ def test_small_layers_stagewise(name):
     inp = L.device_inputs(w)
     cfg = L.layer_config(w, inp)
     gpu = L.run_stages(cfg, inp)
-    summary = L.check_layer(cfg, inp, gpu)
+    summary = L.check_layer(cfg, inp, gpu, bound="rounding")
     assert summary["routing_diff"] == 0 or summary["near_ties"] > 0
 
 
@@ -187,11 +194,11 @@ def test_host_errors_launch_nothing():
 
 # ------------------------------------------------ the named workloads ----
 FULL_SAMPLE = {"mixtral_prefill": 24, "mixtral_decode": 16, "deepseek_fine": 8,
-               "switch_skewed": 48}
+               "deepseek_shared": 8, "switch_skewed": 48}
 
 
 @pytest.mark.parametrize("name", ["mixtral_decode", "switch_skewed", "mixtral_prefill",
-                                  "deepseek_fine"])
+                                  "deepseek_fine", "deepseek_shared"])
 def test_full_size_workload(name):
     w = moe_inputs.WORKLOADS[name]
     cfg = moe.LayerConfig.from_workload(w)
@@ -280,7 +287,8 @@ def _random_workloads(n=24, seed=2024):
                                add_residual=bool(rng.integers(0, 2)),
                                router_bias=str(rng.choice(["none", "uniform"])),
                                gate_mode=str(rng.choice(["renorm", "renorm", "softmax"])),
-                               select_bias=str(rng.choice(["none", "none", "uniform"]))))
+                               select_bias=str(rng.choice(["none", "none", "uniform"])),
+                               n_shared=int(rng.choice([0, 0, 0, 1, 2]))))
     return out
 
 
