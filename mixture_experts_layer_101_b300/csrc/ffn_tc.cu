@@ -703,10 +703,13 @@ bool set_smem_attr() {
 }
 
 // CTA pairs pay off when experts have several 128-row tiles (then both CTAs
-// of a pair compute stored rows); with about one tile per expert the odd CTA
-// would mostly compute discarded rows.
-bool use_pairs(const moe_config& c, int64_t rows) {
-  return rows >= static_cast<int64_t>(c.n_experts + c.n_shared) * BM * 4;
+// of a pair compute stored rows; with about one tile per expert the odd CTA
+// would mostly compute discarded rows) and the reduction is long enough to
+// amortise the pair's coupling per tile (measured: with 16 K-steps per tile,
+// the Switch-shaped gate/up GEMM, one CTA per tile is 12 % faster; with 64
+// and more, pairs win).
+bool use_pairs(const moe_config& c, int64_t rows, int kdim) {
+  return rows >= static_cast<int64_t>(c.n_experts + c.n_shared) * BM * 4 && kdim >= 2048;
 }
 
 template <int MODE>
@@ -737,58 +740,60 @@ bool ffn_tc_supported(const moe_config& c) {
          c.d_ff % 128 == 0 && c.n_experts + c.n_shared <= MAX_EXPERTS;
 }
 
-moe_status launch_ffn_tc(const moe_config& c, int64_t a_max, const void* x_perm,
+moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w, void* h, float* o,
                          uint32_t* status, cudaStream_t s, int part) {
-  if (a_max == 0) return MOE_OK;
-  const int N = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
-  const bool pairs = use_pairs(c, a_max);
-  CUtensorMap mx, mg, mu, mh, md;
-  if (!make_map(&mx, x_perm, a_max, d, 128) ||
-      !make_map(&mg, w.w_gate, static_cast<uint64_t>(N) * F, d, 128) ||
-      !make_map(&mu, w.w_up, static_cast<uint64_t>(N) * F, d, 128) ||
-      !make_map(&mh, h, a_max, F, 128) ||
-      !make_map(&md, w.w_down, static_cast<uint64_t>(N) * d, F, pairs ? 128 : 256))
-    return MOE_ERR_CUDA;
+  if (rows == 0) return MOE_OK;
+  const int E = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
+  const bool pairs1 = use_pairs(c, rows, d);  // gate/up: reduction over d
+  const bool pairs2 = use_pairs(c, rows, F);  // down: reduction over F
   if (!set_smem_attr()) return MOE_ERR_CUDA;
-  const int64_t mtiles = N + (a_max + BM - 1) / BM;  // upper bound on (expert, m-tile) pairs
+  const int64_t mtiles = E + (rows + BM - 1) / BM;       // upper bound on (expert, m-tile)
+  const int64_t ptiles = E + (rows + 2 * BM - 1) / (2 * BM);
   const int sms = sm_count();
-  CUtensorMap mx64, mx32, mx16, mh64, mh32, mh16;  // A boxes for partly filled tiles
-  if (!pairs && (!make_map(&mx64, x_perm, a_max, d, 64) || !make_map(&mx32, x_perm, a_max, d, 32) ||
-                 !make_map(&mx16, x_perm, a_max, d, 16) || !make_map(&mh64, h, a_max, F, 64) ||
-                 !make_map(&mh32, h, a_max, F, 32) || !make_map(&mh16, h, a_max, F, 16)))
-    return MOE_ERR_CUDA;
-  if (pairs) {
-    const int64_t ptiles = N + (a_max + 2 * BM - 1) / (2 * BM);
-    if (part & 1) {
-      TcArgs a1{offsets, N, d, F / 128, F, h, F, status};
+  if (part & 1) {
+    CUtensorMap mx, mg, mu;
+    if (!make_map(&mx, x_perm, rows, d, 128) ||
+        !make_map(&mg, w.w_gate, static_cast<uint64_t>(E) * F, d, 128) ||
+        !make_map(&mu, w.w_up, static_cast<uint64_t>(E) * F, d, 128))
+      return MOE_ERR_CUDA;
+    TcArgs a1{offsets, E, d, F / 128, F, h, F, status};
+    if (pairs1) {
       if (launch_pair<0>(mx, mg, mu, a1, ptiles * (F / 128), s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    }
-    if (part & 2) {
-      TcArgs a2{offsets, N, F, d / 256, d, o, d, status};
-      if (launch_pair<1>(mh, md, md, a2, ptiles * (d / 256), s) != cudaSuccess)
+    } else {
+      CUtensorMap mx64, mx32, mx16;  // activation boxes for partly filled tiles
+      if (!make_map(&mx64, x_perm, rows, d, 64) || !make_map(&mx32, x_perm, rows, d, 32) ||
+          !make_map(&mx16, x_perm, rows, d, 16))
         return MOE_ERR_CUDA;
+      const int64_t t1 = mtiles * (F / 128);
+      grouped_gemm_tc<0, 128><<<static_cast<unsigned>(t1 < sms ? t1 : sms), kThreads,
+                                TcShape<0, 128>::SMEM, s>>>(mx, mg, mu, mx64, mx32, mx16, a1);
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }
-    return MOE_OK;
-  }
-  if (part & 1) {
-    TcArgs a1{offsets, N, d, F / 128, F, h, F, status};
-    const int64_t t1 = mtiles * (F / 128);
-    grouped_gemm_tc<0, 128><<<static_cast<unsigned>(t1 < sms ? t1 : sms), kThreads,
-                              TcShape<0, 128>::SMEM, s>>>(mx, mg, mu, mx64, mx32, mx16, a1);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (part & 2) {
-    TcArgs a2{offsets, N, F, d / 256, d, o, d, status};
-    const int64_t t2 = mtiles * (d / 256);
-    grouped_gemm_tc<1, 128><<<static_cast<unsigned>(t2 < sms ? t2 : sms), kThreads,
-                              TcShape<1, 128>::SMEM, s>>>(mh, md, md, mh64, mh32, mh16, a2);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    CUtensorMap mh, md;
+    if (!make_map(&mh, h, rows, F, 128) ||
+        !make_map(&md, w.w_down, static_cast<uint64_t>(E) * d, F, pairs2 ? 128 : 256))
+      return MOE_ERR_CUDA;
+    TcArgs a2{offsets, E, F, d / 256, d, o, d, status};
+    if (pairs2) {
+      if (launch_pair<1>(mh, md, md, a2, ptiles * (d / 256), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else {
+      CUtensorMap mh64, mh32, mh16;
+      if (!make_map(&mh64, h, rows, F, 64) || !make_map(&mh32, h, rows, F, 32) ||
+          !make_map(&mh16, h, rows, F, 16))
+        return MOE_ERR_CUDA;
+      const int64_t t2 = mtiles * (d / 256);
+      grouped_gemm_tc<1, 128><<<static_cast<unsigned>(t2 < sms ? t2 : sms), kThreads,
+                                TcShape<1, 128>::SMEM, s>>>(mh, md, md, mh64, mh32, mh16, a2);
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
   }
   return MOE_OK;
 }
-
 }  // namespace moe
 
 // ---------------------------------------------------------------------------

@@ -44,6 +44,11 @@ SMALL = {
     "tc_many_tiles_capacity": wl(T=3000, d=512, F=128, N=4, K=1, capacity_factor=1.1,
                             router_bias="skew", add_residual=True),
     "tc_many_tiles_uneven": wl(T=2600, d=256, F=384, N=3, K=2, router_bias="skew"),
+    # CTA pairs (several tiles per expert and a reduction of >= 2048): both
+    # GEMMs in pairs; gate/up on one CTA per tile and down in pairs
+    "tc_pairs_both": wl(T=1500, d=2048, F=2048, N=2, K=2),
+    "tc_pairs_down_only": wl(T=2048, d=1024, F=2048, N=2, K=1, n_shared=1,
+                             capacity_factor=1.5, add_residual=True),
     # enough tiles for the wide (128+128 column) gate/up tile of the one-CTA kernel
     "tc_wide_tiles": wl(T=4096, d=256, F=1280, N=64, K=2),
     # gate variants: full-softmax (Switch) gates, top-K selection bias
