@@ -90,7 +90,7 @@ WsLayout ws_layout(const moe_config* c) {
   L.pcnt = take(nr * N * 4);
   const RouterTcPlan rp = router_tc_plan(*c);
   L.w3 = take(rp.use ? static_cast<size_t>(3) * rp.NP * d * 2 : 0);
-  L.part = take(rp.use ? static_cast<size_t>(rp.S) * T * rp.NP * 4 : 0);
+  L.part = take(rp.use && !rp.fused ? static_cast<size_t>(rp.S) * T * rp.NP * 4 : 0);
   L.ghist = take(K * nd * N * 4);
   L.gbase = take(K * nd * N * 4);
   L.offsets = take((N + S + 1) * 4);
@@ -196,7 +196,9 @@ int32_t moe_capacity(const moe_config* cfg) {
 int32_t moe_forward_launch_count(const moe_config* cfg) {
   if (!config_valid(cfg, nullptr)) return -1;
   if (cfg->T == 0) return 1;  // the dispatch scan still writes offsets and counts
-  const int router = router_tc_plan(*cfg).use ? 3 : 1;  // (split, GEMM, top-K) or fused
+  const RouterTcPlan rp = router_tc_plan(*cfg);
+  // tensor cores: weight split, GEMM (+ top-K unless fused); else one CUDA-core kernel
+  const int router = rp.use ? (rp.fused ? 2 : 3) : 1;
   const int stats = 2;                                  // per-expert reduction, L_aux
   const int dispatch = 4;                               // histogram, scan, permute, gather
   const int ffn = 2;                                    // gate/up, down

@@ -80,10 +80,13 @@ int sm_count();
 
 // ---- launchers (each returns MOE_OK or MOE_ERR_CUDA) -----------------------
 // Tensor-core router plan: NP = experts padded to 32/64/128/256, NPT = experts
-// per tile, S = K splits of kb_per_split 64-wide steps each.
+// per tile, S = K splits of kb_per_split 64-wide steps each. fused: one split
+// and one expert tile, so selection runs in the GEMM epilogue (no partial
+// logits, no top-K kernel). stat_blocks: the per-block statistics partials the
+// router leaves (one per 128-token tile when fused, else one per 32 tokens).
 struct RouterTcPlan {
-  bool use;
-  int NP, NPT, S, kb_per_split;
+  bool use, fused;
+  int NP, NPT, S, kb_per_split, stat_blocks;
 };
 RouterTcPlan router_tc_plan(const moe_config& c);
 

@@ -245,7 +245,9 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
   float* psum = sc.psum;
   int32_t* pcnt = sc.pcnt;
   const RouterTcPlan plan = router_tc_plan(c);
-  if (plan.use && sc.w3 != nullptr && sc.part != nullptr) {
+  int nblk = (c.T + BM - 1) / BM;  // statistics partials left by the router
+  if (plan.use && sc.w3 != nullptr && (plan.fused || sc.part != nullptr)) {
+    nblk = plan.stat_blocks;
     const moe_status r = launch_router_tc(c, plan, x, w_r, b_r, idx, gate, sc.w3, sc.part, psum,
                                           pcnt, status, s);
     if (r != MOE_OK) return r;
@@ -260,7 +262,6 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (st && (st->count || st->f || st->P || st->l_aux || st->z_loss || st->entropy)) {
-    const int nblk = (c.T + BM - 1) / BM;
     route_stats_kernel<<<c.n_experts + 2, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts,
                                                        c.top_k, st->count, st->f, st->P,
                                                        st->z_loss, st->entropy);

@@ -50,11 +50,13 @@ constexpr int kTargetCtas = 148;  // split K until the grid roughly fills a B300
 constexpr int kMaxSplits = 16;
 constexpr int kChunkKb = 2;  // 64-wide K steps per TMEM accumulation chain
 
-template <int NPT>
+// FUSED kernels keep two stages, so that two CTAs share an SM (NPT <= 64) and
+// one CTA's selection epilogue overlaps the other's main loop.
+template <int NPT, bool FUSED>
 struct Shape {
   static constexpr int B_PLANE = NPT * BK * 2;           // one plane's tile
   static constexpr int STAGE = A_BYTES + 3 * B_PLANE;     // x tile + 3 planes
-  static constexpr int STAGES = (NPT == 128) ? 3 : (NPT == 64 ? 5 : 6);
+  static constexpr int STAGES = FUSED ? 2 : ((NPT == 128) ? 3 : (NPT == 64 ? 5 : 6));
   static constexpr int TMEM_COLS = 2 * NPT;  // two chunk accumulators
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int SMEM = 1024 + STAGES * STAGE + NUM_BARS * 8 + 16;
@@ -81,16 +83,164 @@ router_split_kernel(const float* __restrict__ w_r, int N, int NP, int d,
 
 struct GemmArgs {
   int T, NP, KB, kb_per_split;
-  float* part;  // [S][T][NP]
+  float* part;  // [S][T][NP] (unfused)
   uint32_t* status;
+  // fused selection (one K split, all experts in one tile)
+  int N, K, gate_mode;
+  const float* b_r;
+  const float* sel_bias;
+  int32_t* idx;
+  float* gate;
+  float* psum;   // [N+2][nblk], nblk = ceil(T/128)
+  int32_t* pcnt; // [N][nblk]
 };
 
+// ---- fused selection in the GEMM epilogue ----------------------------------
+// Scratch in the drained stage buffers: p[128][NPT + 1] (the block's softmax
+// rows; the odd row pitch keeps both the row writes and the column reads free
+// of bank conflicts), zh[2][128] (per-token squared log-sum-exp and entropy),
+// cnt[NPT] (assignment counts).
 template <int NPT>
+struct FusedScratch {
+  float* p;
+  float* zh;
+  int32_t* cnt;
+  __device__ explicit FusedScratch(uint8_t* base)
+      : p(reinterpret_cast<float*>(base)),
+        zh(p + 128 * (NPT + 1)),
+        cnt(reinterpret_cast<int32_t*>(zh + 256)) {}
+  static constexpr int BYTES = (128 * (NPT + 1) + 256 + NPT) * 4;
+};
+
+// One token per thread: v holds the token's NPT accumulated logits (entries
+// >= N unused). Top-K first, on the biased selection keys (ties to the lower
+// index), then the softmax, whose exponentials overwrite v. Same arithmetic
+// as route_one_token, serial instead of across a warp.
+__device__ __forceinline__ void epilogue_bar() {  // the 128 epilogue threads
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <int NPT>
+__device__ __forceinline__ void fused_select(float (&v)[NPT], const GemmArgs& a, int t, int row,
+                                             const FusedScratch<NPT>& sc) {
+  const int N = a.N, K = a.K;
+  float* prow = sc.p + row * (NPT + 1);
+  if (t >= a.T) {  // past the last token: contributes nothing
+#pragma unroll
+    for (int e = 0; e < NPT; ++e) prow[e] = 0.f;
+    sc.zh[row] = 0.f;
+    sc.zh[128 + row] = 0.f;
+    return;
+  }
+  float mx = -INFINITY;
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < NPT; ++e) {
+    if (e < N) {
+      if (a.b_r != nullptr) v[e] += a.b_r[e];
+      if (!isfinite(v[e])) bad = true;
+      mx = fmaxf(mx, v[e]);
+    }
+  }
+  if (bad) set_status(a.status, MOE_ERR_NONFINITE);
+  // top-K
+  uint32_t taken[(NPT + 31) / 32];
+#pragma unroll
+  for (int i = 0; i < (NPT + 31) / 32; ++i) taken[i] = 0u;
+  int sel_e[8];
+  float sel_u[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // unrolled: constant indices keep sel_* in registers
+    sel_e[k] = 0;
+    sel_u[k] = -INFINITY;
+    if (k >= K) continue;
+    float bv = -INFINITY, bu = -INFINITY;
+    int be = -1;
+#pragma unroll
+    for (int e = 0; e < NPT; ++e) {
+      if (e >= N || ((taken[e >> 5] >> (e & 31)) & 1u)) continue;
+      const float u = isnan(v[e]) ? -INFINITY : v[e];
+      const float key = a.sel_bias != nullptr ? u + a.sel_bias[e] : u;
+      if (be < 0 || key > bv) {
+        bv = key;
+        be = e;
+        bu = v[e];
+      }
+    }
+    if (be < 0) be = 0;  // unreachable while K <= N; keeps indices in range
+#pragma unroll
+    for (int i = 0; i < (NPT + 31) / 32; ++i)
+      if (i == (be >> 5)) taken[i] |= 1u << (be & 31);
+    sel_e[k] = be;
+    sel_u[k] = bu;
+  }
+  // softmax over the N experts
+  float sum = 0.f, pv = 0.f;
+#pragma unroll
+  for (int e = 0; e < NPT; ++e) {
+    if (e < N) {
+      const float ex = expf(v[e] - mx);
+      sum += ex;
+      if (ex > 0.f) pv += ex * v[e];
+      v[e] = ex;
+    }
+  }
+  const float inv = 1.f / sum;
+#pragma unroll
+  for (int e = 0; e < NPT; ++e) prow[e] = e < N ? v[e] * inv : 0.f;
+  const float lse = mx + logf(sum);
+  sc.zh[row] = lse * lse;
+  sc.zh[128 + row] = lse - pv * inv;
+  // gates
+  float msel = sel_u[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k)
+    if (k < K) msel = fmaxf(msel, sel_u[k]);
+  float gsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < K) gsum += expf(sel_u[k] - msel);
+  const size_t t0 = static_cast<size_t>(t) * K;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (k >= K) break;
+    a.idx[t0 + k] = sel_e[k];
+    a.gate[t0 + k] = a.gate_mode == MOE_GATE_SOFTMAX ? expf(sel_u[k] - mx) * inv
+                                                     : expf(sel_u[k] - msel) / gsum;
+    atomicAdd(&sc.cnt[sel_e[k]], 1);
+  }
+}
+
+// The block's partial statistics, in the layout write_block_stats uses
+// (psum[e][blk], pcnt[e][blk], psum[N][blk] and psum[N+1][blk]), rows summed
+// in ascending order; one column per thread.
+template <int NPT>
+__device__ __forceinline__ void fused_block_stats(const GemmArgs& a, int m, int row,
+                                                  const FusedScratch<NPT>& sc) {
+  const size_t nblk = gridDim.x;
+  for (int j = row; j < a.N + 2; j += 128) {
+    float s = 0.f;
+    if (j < a.N) {
+      for (int r = 0; r < 128; ++r) s += sc.p[r * (NPT + 1) + j];
+      a.pcnt[static_cast<size_t>(j) * nblk + m] = sc.cnt[j];
+    } else {
+      for (int r = 0; r < 128; ++r) s += sc.zh[(j - a.N) * 128 + r];
+    }
+    a.psum[static_cast<size_t>(j) * nblk + m] = s;
+  }
+}
+
+// FUSED: one K split and all experts in one tile, so the thread that owns a
+// token's TMEM row holds all of its logits; it then runs softmax, top-K,
+// gates and the block's statistics partials itself (the whole router in one
+// kernel), using the drained stage buffers as scratch.
+template <int NPT, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
 router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                const GemmArgs args) {
   using namespace ptx;
-  using S = Shape<NPT>;
+  using S = Shape<NPT, FUSED>;
+  static_assert(!FUSED || FusedScratch<NPT>::BYTES <= S::STAGES * S::STAGE, "scratch");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -121,6 +271,7 @@ router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
+    tmem_slot[2] = 0;  // epilogue failure flag (FUSED)
     fence_mbar_init();
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
@@ -242,7 +393,7 @@ router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     if (!ok) {
       if (lane == 0) fail();
-    } else {
+    } else if (!FUSED) {
       const int t = m * BM + q * 32 + lane;
       if (t < args.T) {
         float4* dst = reinterpret_cast<float4*>(
@@ -252,6 +403,23 @@ router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         for (int j = 0; j < NPT / 4; ++j)
           dst[j] = make_float4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
       }
+    }
+    if (FUSED) {
+      // Every epilogue thread passes the same three named barriers whatever
+      // happened, so a timeout in one warp leaves no other warp waiting; the
+      // selection runs only if all four warps saw every chunk, which also
+      // means every MMA has finished reading the stage buffers.
+      volatile int* epi_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);
+      const FusedScratch<NPT> sc(gbase);
+      const int row = q * 32 + lane;
+      if (!ok && lane == 0) *epi_fail = 1;
+      epilogue_bar();
+      const bool all_ok = *epi_fail == 0;
+      if (all_ok && row < NPT) sc.cnt[row] = 0;
+      epilogue_bar();
+      if (all_ok) fused_select<NPT>(run, args, m * BM + row, row, sc);
+      epilogue_bar();
+      if (all_ok) fused_block_stats<NPT>(args, m, row, sc);
     }
   }
   tc_fence_before();
@@ -330,7 +498,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NPT>
+template <int NPT, bool FUSED>
 cudaError_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, const GemmArgs& a,
                         dim3 grid, cudaStream_t s) {
   static std::mutex mu;
@@ -341,12 +509,13 @@ cudaError_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, const Gemm
     std::lock_guard<std::mutex> lock(mu);
     if (!(dev < 31 && (done_mask >> dev) & 1)) {
       const cudaError_t e = cudaFuncSetAttribute(
-          router_gemm_tc<NPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Shape<NPT>::SMEM);
+          router_gemm_tc<NPT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          Shape<NPT, FUSED>::SMEM);
       if (e != cudaSuccess) return e;
       if (dev < 31) done_mask |= 1 << dev;
     }
   }
-  router_gemm_tc<NPT><<<grid, kThreads, Shape<NPT>::SMEM, s>>>(mx, mw, a);
+  router_gemm_tc<NPT, FUSED><<<grid, kThreads, Shape<NPT, FUSED>::SMEM, s>>>(mx, mw, a);
   return cudaGetLastError();
 }
 
@@ -366,6 +535,10 @@ RouterTcPlan router_tc_plan(const moe_config& c) {
   S = S > KB ? KB : S;
   p.kb_per_split = (KB + S - 1) / S;
   p.S = (KB + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
+  // one split and one expert tile: the GEMM epilogue holds whole tokens
+  p.fused = p.S == 1 && p.NP == p.NPT;
+  p.stat_blocks = p.fused ? (c.T + BM - 1) / BM
+                          : (c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
   return p;
 }
 
@@ -380,12 +553,19 @@ moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const vo
   if (!make_map(&mx, x, static_cast<uint64_t>(T), d, BM) ||
       !make_map(&mw, w3, static_cast<uint64_t>(3) * p.NP, d, p.NPT))
     return MOE_ERR_CUDA;
-  GemmArgs a{T, p.NP, d / BK, p.kb_per_split, part, status};
+  GemmArgs a{T, p.NP, d / BK, p.kb_per_split, part, status, N, c.top_k, c.gate_mode, b_r,
+             c.select_bias, idx, gate, psum, pcnt};
   const dim3 grid((T + BM - 1) / BM, p.NP / p.NPT, p.S);
   cudaError_t e;
-  if (p.NPT == 128) e = launch_gemm<128>(mx, mw, a, grid, s);
-  else if (p.NPT == 64) e = launch_gemm<64>(mx, mw, a, grid, s);
-  else e = launch_gemm<32>(mx, mw, a, grid, s);
+  if (p.fused) {
+    if (p.NPT == 128) e = launch_gemm<128, true>(mx, mw, a, grid, s);
+    else if (p.NPT == 64) e = launch_gemm<64, true>(mx, mw, a, grid, s);
+    else e = launch_gemm<32, true>(mx, mw, a, grid, s);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  if (p.NPT == 128) e = launch_gemm<128, false>(mx, mw, a, grid, s);
+  else if (p.NPT == 64) e = launch_gemm<64, false>(mx, mw, a, grid, s);
+  else e = launch_gemm<32, false>(mx, mw, a, grid, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
   if (N <= 32)

@@ -124,6 +124,10 @@ def test_launch_count(lib):
     assert moe.forward_launch_count(cfg(dtype="f32")) == 10
     assert moe.forward_launch_count(cfg(d_model=72)) == 10  # d % 64 != 0: CUDA-core router
     assert moe.forward_launch_count(cfg(top_k=9, n_experts=16)) == -1
+    # one K split and one expert tile: selection runs in the router GEMM epilogue
+    assert moe.forward_launch_count(cfg(T=32768, d_model=1024, n_experts=64, top_k=1)) == 11
+    assert moe.forward_launch_count(cfg(T=100, d_model=64)) == 11
+    assert moe.forward_launch_count(cfg(T=4096, n_experts=256, top_k=8)) == 12  # two tiles
 
 
 def test_tensor_core_path_choice(lib):

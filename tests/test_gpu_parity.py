@@ -65,6 +65,14 @@ SMALL = {
     "tc_shared_pairs": wl(T=2048, d=256, F=256, N=2, K=1, n_shared=1),
     "simt_shared_gelu_fp32": wl(T=90, d=64, F=96, N=4, K=2, n_shared=2, dtype="f32",
                                 activation="gelu", has_bias=True, init="uniform"),
+    # router selection fused into the tensor-core router's epilogue (one K
+    # split and one expert tile): 32-, 64- and 128-wide expert tiles, ragged
+    # expert counts and token tails, several accumulation chunks
+    "fused_router_n8": wl(T=1000, d=64, F=128, N=8, K=2),
+    "fused_router_n100_top8_bias": wl(T=777, d=64, F=64, N=100, K=8, select_bias="uniform"),
+    "fused_router_switch_gate": wl(T=2000, d=64, F=64, N=64, K=1, gate_mode="softmax",
+                                   capacity_factor=1.25, add_residual=True, router_bias="skew"),
+    "fused_router_chunks": wl(T=19500, d=256, F=64, N=40, K=2, router_bias="uniform"),
     # CUDA-core path: fp32, GELU, or shapes the tensor-core kernel does not tile
     "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
     "simt_gelu_nobias": wl(T=90, d=64, F=96, N=4, K=2, dtype="f32", activation="gelu",
