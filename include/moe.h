@@ -14,7 +14,8 @@
  *                  (learnagent.wiki): 结构 2 路由器, 结构 3 Top-K 选择与输出融合,
  *                  运行示例 (minimal MoELayer).
  *   [替代FFN]      "MoE 如何替代 FFN？它解决了什么问题？带来哪些新挑战？"
- *                  (mstx.cn/posts/467.html): §1 标准 FFN, §2 MoE 如何替代 FFN.
+ *                  (mstx.cn/posts/467.html): §1 标准 FFN, §2 MoE 如何替代 FFN,
+ *                  §4 (3) 路由与梯度.
  *
  * Notation: T tokens, d = d_model, N routed experts, S shared experts,
  * K = top-K, F = d_ff, C = per-expert capacity, A = number of kept
@@ -102,6 +103,11 @@ typedef struct {
                            routed ones in every weight array; each takes every
                            token with gate 1, outside the router, the capacity
                            and the statistics ([替代FFN] §5, DeepSeek-MoE)     */
+  int32_t save_for_backward; /* 1: moe_forward also keeps in the workspace
+                           what moe_backward needs (router logits [T][N] fp32,
+                           the expert pre-activations [R_max][2F] in cfg->dtype,
+                           the counts) and moe_workspace_size grows by those
+                           and by moe_backward's scratch; 0: inference only  */
 } moe_config;
 
 /* Device-side statistics; every member is a caller-owned DEVICE pointer and
@@ -150,7 +156,10 @@ typedef struct {
 /* Bytes of workspace that moe_forward needs for cfg (an upper bound for the
  * other entry points too). Pure host function; returns 0 if cfg is invalid.
  * It covers x_perm [R_max][d], h [R_max][F] and o [R_max][d] fp32, where
- * A_max = min(T*K, N*C) and R_max = A_max + S*T. */
+ * A_max = min(T*K, N*C) and R_max = A_max + S*T; with
+ * cfg->save_for_backward also the saved state and the scratch of
+ * moe_backward (pre-activations and output gradients [R_max][2F] and
+ * [R_max][d] in cfg->dtype, logits and their gradient [T][N] fp32). */
 size_t moe_workspace_size(const moe_config* cfg);
 
 /* Capacity C per expert: floor(K * CF * T / N), computed exactly on the
@@ -262,11 +271,63 @@ moe_status moe_combine(const moe_config* cfg, const float* o,
  * [稀疏激活原理] §三 MoELayer.forward; [概念卡] 核心原理 (four steps).
  *   x [T][d], w_r [N][d] fp32, b_r [N] fp32 or NULL, weights as above,
  *   y [T][d] (out), stats (all members optional), ws >= moe_workspace_size.
+ *   With T = 0, x and y may be NULL.
  * Errors: the union of the above. */
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r,
                        const float* b_r, const moe_expert_weights* weights,
                        void* y, moe_stats* stats, void* ws,
                        moe_stream_t stream);
+
+/* Gradients written by moe_backward: caller-owned DEVICE fp32 buffers, each
+ * overwritten (not accumulated). E = N + S; shapes follow the weights.
+ *   dx [T][d] and dw_r [N][d] are required; db_r [N] may be NULL.
+ *   SwiGLU: dw_gate [E][F][d], dw_up [E][F][d], dw_down [E][d][F].
+ *   GELU:   dw1 [E][F][d], dw2 [E][d][F]; db1 [E][F], db2 [E][d] iff
+ *           cfg->has_bias. Members of the other activation are ignored.   */
+typedef struct {
+  float* dx;
+  float* dw_r;
+  float* db_r;
+  float* dw_gate;
+  float* dw_up;
+  float* dw_down;
+  float* dw1;
+  float* db1;
+  float* dw2;
+  float* db2;
+} moe_grads;
+
+/* Backward pass: the gradients of the training objective
+ *   L = sum_{t,j} dy[t][j] * y[t][j] + L_aux + z_coef * z_loss
+ * (dy = dLoss/dy of whatever follows the layer; L_aux = alpha*N*sum f*P and
+ * z_loss as reported in moe_stats) with respect to x, W_r, b_r and every
+ * expert weight. The top-K choice, the capacity truncation and the selection
+ * bias are piecewise constant and pass no gradient ([稀疏激活原理] §四
+ * 训练不稳定性: the expert choice itself has zero gradient, the gate softmax
+ * is differentiable; [替代FFN] §4 (3)); f is a count and passes none, P
+ * carries L_aux's gradient ([稀疏激活原理] §2.2); the router receives
+ * gradient through the gates, P and the z-loss ([概念卡] 结构 2: trained end
+ * to end); a dropped assignment passes none; shared experts receive dy.
+ * Steps (all on the GPU): gate and output gradients of the combine; logit
+ * gradient; per expert, the down projection's input and weight gradients
+ * (with the activation's derivative), the first projection's input and
+ * weight gradients; dx = residual + sum of the expert input gradients +
+ * dlogits W_r; dW_r = dlogits^T x.
+ * Precondition: ws holds the state of the latest moe_forward with the same
+ * cfg (save_for_backward = 1), x, w_r, b_r and weights, unchanged since.
+ *   x [T][d] cfg->dtype, w_r [N][d] fp32, weights as in moe_forward,
+ *   dy [T][d] cfg->dtype, z_coef >= 0 (finite), grads as above (x, dy and
+ *   grads->dx may be NULL when T = 0; every weight gradient is then zero).
+ * Intermediate gradients are rounded to cfg->dtype where they feed a
+ * tensor-core product (the expert output gradient g*dy and the
+ * pre-activation gradients), as the forward rounds h.
+ * Errors: MOE_ERR_INVALID (NULL or misaligned pointers, z_coef not finite or
+ * negative, cfg->save_for_backward == 0), MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_WORKSPACE, MOE_ERR_CUDA; device: MOE_ERR_TIMEOUT. */
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* w_r,
+                        const moe_expert_weights* weights, const void* dy,
+                        float z_coef, moe_grads* grads, moe_stats* stats,
+                        void* ws, moe_stream_t stream);
 
 /* Tracing (instrumentation; the pages have no counterpart). Registers up to
  * 6 caller-created CUDA events (cudaEvent_t, passed as void*) for the
@@ -296,6 +357,11 @@ const char* moe_status_string(moe_status s);
  * of stats non-NULL), for accounting by benchmarks and tracers; -1 if cfg
  * is invalid. Instrumentation; the pages have no counterpart. */
 int32_t moe_forward_launch_count(const moe_config* cfg);
+
+/* Number of kernels one moe_backward call on cfg launches (with db_r
+ * non-NULL; two fewer without it, none for T = 0); -1 if cfg is invalid or
+ * has save_for_backward == 0. Instrumentation. */
+int32_t moe_backward_launch_count(const moe_config* cfg);
 
 /* 1 if the expert FFN of cfg runs on the tcgen05 tensor-core path, 0 if it
  * runs on the CUDA-core path (fp32 configurations, or shapes whose d is not a

@@ -1,0 +1,547 @@
+// Expert gradients of the backward pass on the tcgen05 tensor cores (bf16
+// SwiGLU layers whose forward runs on the tensor cores).
+//
+// Sources: the derivatives of "MoE 混合专家模型稀疏激活的架构原理与负载均衡挑战"
+// §三 class Expert (down(silu(gate(x)) * up(x))), trained end to end with the
+// router ("混合专家模型（Mixture of Experts, MoE）" 结构 2).
+//
+// For the rows r of expert e ([offsets[e], offsets[e+1]), routed experts
+// then shared ones), with a | b the kept gate | up pre-activations, h the
+// forward's hidden activation and dout the output gradient g * dy:
+//   DGRAD_SWIGLU  dh[r][f] = sum_j dout[r][j] W_down[e][j][f], and in the
+//                 epilogue (da, db) = (dh b silu'(a), dh silu(a)) written
+//                 over (a, b) in place (bf16)
+//   WGRAD         dW_down[e][j][f] = sum_r dout[r][j] h[r][f]
+//   DGRAD_STORE   dx_perm[r][j] = sum_f da[r][f] W_gate[e][f][j]
+//                                + sum_f db[r][f] W_up[e][f][j]   (fp32)
+//   WGRAD         dW_gate[e][f][j] = sum_r da[r][f] x_perm[r][j] and
+//                 dW_up[e][f][j] = sum_r db[r][f] x_perm[r][j]: one launch
+//                 over M = 2F rows of (da | db)
+// The weights enter the dgrad products with their output dimension
+// contiguous, and both operands of the weight-gradient products have their
+// M / N dimension contiguous along the token rows, so those operands are
+// loaded as MN-major tiles (the TMA box is 64 columns x 64 rows; the MMA
+// reads 64-column slices 8 KB apart); only the dgrad A operand is K-major.
+//
+// Kernel: persistent and warp-specialised like the forward's grouped GEMM
+// (warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue, two TMEM
+// accumulators of BN fp32 columns). DGRAD tiles are (expert, 128-row tile,
+// BN-column tile); a row tile may run past its expert's rows, whose
+// accumulator rows are never stored. WGRAD tiles are (expert, 128-row
+// block of M, BN-column block); the reduction runs over the expert's token
+// rows in 64-row steps, and in the last step the MMA warp zeroes the A rows
+// that lie past the expert (they belong to the next expert) before the MMA
+// reads them. An expert with no rows gets zeros. Every wait is bounded.
+#include "moe_common.cuh"
+#include "ptx_sm100.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BK = 64, kThreads = 192;
+constexpr int MAX_GROUPS = 264;
+constexpr int CHUNK = 64 * 128;  // one 64-column x 64-row MN-major box: 8 KB
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+enum { DGRAD_STORE = 0, DGRAD_SWIGLU = 1, WGRAD = 2 };
+
+template <int KIND, int BN>
+struct BwShape {
+  static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+  static constexpr int B_BYTES = BN * BK * 2;  // 16 or 32 KB
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE) > 6 ? 6 : (196608 / STAGE);
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + NUM_BARS * 8 + 16 + 2 * (MAX_GROUPS + 1) * 4;
+  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32_major(BM, BN, KIND == WGRAD, true);
+};
+
+struct BwArgs {
+  const int32_t* offsets;  // [G+1] row offsets of the experts
+  int groups;
+  int kb_total;            // DGRAD: 64-wide K steps
+  int kb_split;            // DGRAD: K steps read from the first B map (rest: second)
+  int b_rows;              // DGRAD: rows of a B map per expert (its K extent)
+  int n_tiles;             // BN-column tiles per output row block
+  int m_blocks;            // WGRAD: 128-row blocks of M per expert
+  int m_split;             // WGRAD: output rows >= m_split go to out2 (row - m_split)
+  int acol;                // WGRAD: first column of A used
+  float* out;              // DGRAD_STORE: [rows][ldo]; WGRAD: [G][m_split or M][ldo]
+  float* out2;             // WGRAD: second output (dW_up) or NULL
+  int ldo;
+  __nv_bfloat16* pre;      // DGRAD_SWIGLU: [rows][2F] (a | b in, da | db out)
+  int F;
+  uint32_t* status;
+};
+
+template <int KIND, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+               const __grid_constant__ CUtensorMap tmB1, const BwArgs args) {
+  using namespace ptx;
+  using Sh = BwShape<KIND, BN>;
+  constexpr int STAGES = Sh::STAGES;
+  constexpr bool W = KIND == WGRAD;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base, sB = base + STAGES * Sh::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * Sh::STAGE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Sh::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
+  int* seg_off = tile_start + (MAX_GROUPS + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = args.groups;
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto bar_tfull = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
+  auto bar_tempty = [&](int a) { return smem_u32(bars + 2 * STAGES + 2 + a); };
+  const uint32_t bar_drain = smem_u32(bars + 2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull(a), 1);
+      mbar_init(bar_tempty(a), 4);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    if (!W) prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    // tile_start[e]: tiles of experts < e (DGRAD: row tiles x column tiles;
+    // WGRAD: a fixed m_blocks x n_tiles per expert)
+    constexpr int PER = (MAX_GROUPS + 31) / 32;
+    int local[PER], sum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane * PER + j;
+      int tiles = 0;
+      if (e < G) {
+        const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
+        seg_off[e] = o0;
+        tiles = W ? args.m_blocks * args.n_tiles : ((o1 - o0 + BM - 1) / BM) * args.n_tiles;
+      }
+      local[j] = tiles;
+      sum += tiles;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane * PER + j;
+      if (e < G) tile_start[e] = run;
+      run += local[j];
+    }
+    if (lane == 31) tile_start[G] = incl;
+    if (lane == 0) seg_off[G] = args.offsets[G];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tile_start[G];
+
+  // tile -> expert e, row tile / M block m, column tile n
+  auto decode = [&](int tile, int& e, int& m, int& n) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    e = lo;
+    const int local = tile - tile_start[e];
+    if (W) {
+      m = local / args.n_tiles;
+      n = local - m * args.n_tiles;
+    } else {
+      const int mt = (seg_off[e + 1] - seg_off[e] + BM - 1) / BM;
+      n = local / mt;
+      m = local - n * mt;
+    }
+  };
+  auto ksteps = [&](int e) {
+    return W ? (seg_off[e + 1] - seg_off[e] + BK - 1) / BK : args.kb_total;
+  };
+  auto fail = [&]() {
+    set_status(args.status, MOE_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer ----
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_parity = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, m, n;
+      decode(tile, e, m, n);
+      const int nkb = ksteps(e);
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(bar_empty(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_full(stage), Sh::STAGE);
+        const uint32_t a_dst = sA + stage * Sh::A_BYTES, b_dst = sB + stage * Sh::B_BYTES;
+        if (W) {
+          const int r = seg_off[e] + kb * BK;
+#pragma unroll
+          for (int c = 0; c < BM / 64; ++c)
+            tma_load_2d(a_dst + c * CHUNK, &tmA, bar_full(stage), args.acol + m * BM + c * 64, r);
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_2d(b_dst + c * CHUNK, &tmB0, bar_full(stage), n * BN + c * 64, r);
+        } else {
+          tma_load_2d(a_dst, &tmA, bar_full(stage), kb * BK, seg_off[e] + m * BM);
+          const bool first = kb < args.kb_split;
+          const int krow = e * args.b_rows + (first ? kb : kb - args.kb_split) * BK;
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_2d(b_dst + c * CHUNK, first ? &tmB0 : &tmB1, bar_full(stage),
+                        n * BN + c * 64, krow);
+        }
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      fail();
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s))
+          mbar_wait(bar_full(s), (issued_parity >> s) & 1u, kWaitLimitNs, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (whole warp) ----
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued_any = false;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, m, n;
+      decode(tile, e, m, n);
+      const int nkb = ksteps(e);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_tempty(acc), acc_phase ^ 1u, kWaitLimitNs,
+                                              abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < nkb; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_full(stage), phase, kWaitLimitNs, abort_flag));
+        if (!ok) break;
+        const uint32_t a0 = sA + stage * Sh::A_BYTES, b0 = sB + stage * Sh::B_BYTES;
+        if (W) {
+          // rows of the last step past the expert: zero them in A (whole
+          // 128-byte rows, so the swizzle does not matter)
+          const int valid = seg_off[e + 1] - (seg_off[e] + kb * BK);
+          if (valid < BK) {
+            const int nrow = BK - valid;
+            for (int i = lane; i < (BM / 64) * nrow * 8; i += 32) {
+              const int c = i / (nrow * 8), rr = (i / 8) % nrow, q = i % 8;
+              uint8_t* p = gbase + (a0 - base) + c * CHUNK + (valid + rr) * 128 + q * 16;
+              *reinterpret_cast<uint4*>(p) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = W ? sdesc_mnmajor_sw128(a0 + kk * 2048, CHUNK)
+                                  : sdesc_kmajor_sw128(a0 + kk * 32);
+            const uint64_t bd = sdesc_mnmajor_sw128(b0 + kk * 2048, CHUNK);
+            mma_bf16(d_tmem, ad, bd, Sh::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(bar_empty(stage));
+        }
+        __syncwarp();
+        issued_any = true;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(bar_tfull(acc));  // with no step: arrives at once
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      if (lane == 0) {
+        fail();
+        if (issued_any) {
+          mma_commit(bar_drain);
+          mbar_wait(bar_drain, 0, kWaitLimitNs, nullptr);
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue ----
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, m, n;
+      decode(tile, e, m, n);
+      const int cnt = seg_off[e + 1] - seg_off[e];
+      bool ok = mbar_wait(bar_tfull(acc), acc_phase, kWaitLimitNs, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const int r = m * BM + q * 32 + lane;  // row of the tile this thread drains
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+      if (W) {
+        float* dst;
+        if (args.out2 != nullptr && r >= args.m_split)
+          dst = args.out2 + (static_cast<size_t>(e) * args.m_split + (r - args.m_split)) * args.ldo;
+        else
+          dst = args.out + (static_cast<size_t>(e) * (args.out2 ? args.m_split : args.m_blocks * BM) +
+                            r) * args.ldo;
+        dst += n * BN;
+        if (cnt == 0) {
+          for (int c = 0; c < BN; c += 4)
+            *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c * 32, v);
+            tmem_ld_wait();
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        }
+      } else {
+        const bool valid = r < cnt;
+        const size_t grow = static_cast<size_t>(seg_off[e]) + static_cast<size_t>(r);
+        if (KIND == DGRAD_STORE) {
+          float* dst = args.out + grow * args.ldo + n * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c * 32, v);
+            tmem_ld_wait();
+            if (valid) {
+              float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                    __uint_as_float(v[4 * j + 2]),
+                                    __uint_as_float(v[4 * j + 3]));
+            }
+          }
+        } else {
+          // (a, b) -> (dh b silu'(a), dh silu(a)), bf16, in place
+          __nv_bfloat16* pa = args.pre + grow * 2 * args.F + n * BN;
+          __nv_bfloat16* pb = pa + args.F;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c * 32, v);
+            tmem_ld_wait();
+            if (valid) {
+              uint4* qa = reinterpret_cast<uint4*>(pa + c * 32);
+              uint4* qb = reinterpret_cast<uint4*>(pb + c * 32);
+#pragma unroll
+              for (int w4 = 0; w4 < 4; ++w4) {
+                uint4 ua = qa[w4], ub = qb[w4];
+                uint32_t* ea = reinterpret_cast<uint32_t*>(&ua);
+                uint32_t* eb = reinterpret_cast<uint32_t*>(&ub);
+#pragma unroll
+                for (int p2 = 0; p2 < 4; ++p2) {
+                  const float2 a2 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&ea[p2]));
+                  const float2 b2 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&eb[p2]));
+                  const float dh0 = __uint_as_float(v[w4 * 8 + p2 * 2]);
+                  const float dh1 = __uint_as_float(v[w4 * 8 + p2 * 2 + 1]);
+                  const float s0 = 1.f / (1.f + expf(-a2.x)), s1 = 1.f / (1.f + expf(-a2.y));
+                  const __nv_bfloat162 da = __floats2bfloat162_rn(
+                      dh0 * b2.x * s0 * (1.f + a2.x * (1.f - s0)),
+                      dh1 * b2.y * s1 * (1.f + a2.y * (1.f - s1)));
+                  const __nv_bfloat162 db =
+                      __floats2bfloat162_rn(dh0 * a2.x * s0, dh1 * a2.y * s1);
+                  ea[p2] = *reinterpret_cast<const uint32_t*>(&da);
+                  eb[p2] = *reinterpret_cast<const uint32_t*>(&db);
+                }
+                qa[w4] = ua;
+                qb[w4] = ub;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Sh::TMEM_COLS);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 [rows][cols] as a 2-D tensor map, box box_rows x 64 columns,
+// 128-byte swizzle; rows past the end read as zeros.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND, int BN>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                   const BwArgs& args, int64_t tiles_bound, cudaStream_t s) {
+  static std::mutex mu;
+  static int done_mask = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!(dev < 31 && (done_mask >> dev) & 1)) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          grouped_bwd_tc<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          BwShape<KIND, BN>::SMEM);
+      if (e != cudaSuccess) return e;
+      if (dev < 31) done_mask |= 1 << dev;
+    }
+  }
+  const int64_t sms = sm_count();
+  const unsigned grid = static_cast<unsigned>(tiles_bound < sms ? tiles_bound : sms);
+  if (grid == 0) return cudaSuccess;
+  grouped_bwd_tc<KIND, BN><<<grid, kThreads, BwShape<KIND, BN>::SMEM, s>>>(a, b0, b1, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool ffn_bwd_tc_supported(const moe_config& c) {
+  return ffn_tc_supported(c) && c.n_experts + c.n_shared <= MAX_GROUPS;
+}
+
+int ffn_bwd_tc_launches(const moe_config&) { return 4; }
+
+moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, const int32_t* offsets,
+                             const moe_expert_weights& w, const void* x_perm, const void* h,
+                             void* pre, const void* dout, float* dx_perm, const moe_grads& g,
+                             uint32_t* status, cudaStream_t s) {
+  if (!ffn_bwd_tc_supported(c)) return MOE_ERR_UNSUPPORTED;
+  const int E = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;
+  const bool f256 = F % 256 == 0;  // column tile along F
+  if (rows == 0) {
+    // no row at all: the weight gradients are zero
+    const size_t wsz = static_cast<size_t>(E) * F * d * sizeof(float);
+    for (float* m : {g.dw_gate, g.dw_up, g.dw_down})
+      if (cudaMemsetAsync(m, 0, wsz, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  const int64_t mt_bound = E + (rows + BM - 1) / BM;  // (expert, row tile) pairs, upper bound
+  CUtensorMap m_dout128, m_dout64, m_h, m_pre128, m_pre64, m_x, m_wd, m_wg, m_wu;
+  if (!make_map(&m_dout128, dout, rows, d, 128) || !make_map(&m_dout64, dout, rows, d, 64) ||
+      !make_map(&m_h, h, rows, F, 64) || !make_map(&m_pre128, pre, rows, 2 * F, 128) ||
+      !make_map(&m_pre64, pre, rows, 2 * F, 64) || !make_map(&m_x, x_perm, rows, d, 64) ||
+      !make_map(&m_wd, w.w_down, static_cast<uint64_t>(E) * d, F, 64) ||
+      !make_map(&m_wg, w.w_gate, static_cast<uint64_t>(E) * F, d, 64) ||
+      !make_map(&m_wu, w.w_up, static_cast<uint64_t>(E) * F, d, 64))
+    return MOE_ERR_CUDA;
+  cudaError_t err;
+  // 1. dh = dout . W_down, activation derivative in place of (a, b)
+  {
+    BwArgs a{offsets, E, d / BK, d / BK, d, F / (f256 ? 256 : 128), 0, 0, 0, nullptr, nullptr,
+             0, static_cast<__nv_bfloat16*>(pre), F, status};
+    err = f256 ? launch<DGRAD_SWIGLU, 256>(m_dout128, m_wd, m_wd, a, mt_bound * a.n_tiles, s)
+               : launch<DGRAD_SWIGLU, 128>(m_dout128, m_wd, m_wd, a, mt_bound * a.n_tiles, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // 2. dW_down[e] = dout_e^T h_e: M = d, N = F
+  {
+    BwArgs a{offsets, E, 0, 0, 0, F / (f256 ? 256 : 128), d / BM, d, 0, g.dw_down, nullptr, F,
+             nullptr, F, status};
+    const int64_t tiles = static_cast<int64_t>(E) * a.m_blocks * a.n_tiles;
+    err = f256 ? launch<WGRAD, 256>(m_dout64, m_h, m_h, a, tiles, s)
+               : launch<WGRAD, 128>(m_dout64, m_h, m_h, a, tiles, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // 3. dx_perm = da . W_gate + db . W_up: K = 2F (first F from W_gate), N = d
+  {
+    BwArgs a{offsets, E, 2 * F / BK, F / BK, F, d / 256, 0, 0, 0, dx_perm, nullptr, d, nullptr,
+             F, status};
+    err = launch<DGRAD_STORE, 256>(m_pre128, m_wg, m_wu, a, mt_bound * a.n_tiles, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // 4. dW_gate | dW_up [e] = (da | db)_e^T x_perm_e: M = 2F rows split at F, N = d
+  {
+    BwArgs a{offsets, E, 0, 0, 0, d / 256, 2 * F / BM, F, 0, g.dw_gate, g.dw_up, d, nullptr, F,
+             status};
+    const int64_t tiles = static_cast<int64_t>(E) * a.m_blocks * a.n_tiles;
+    err = launch<WGRAD, 256>(m_pre64, m_x, m_x, a, tiles, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

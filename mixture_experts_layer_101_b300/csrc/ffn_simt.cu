@@ -24,7 +24,7 @@ template <typename T, int EPI, typename TOut>
 __global__ void __launch_bounds__(kThreads)
 grouped_gemm_simt(const T* __restrict__ A, const T* __restrict__ B0, const T* __restrict__ B1,
                   const T* __restrict__ bias, const int32_t* __restrict__ offsets, int n_experts,
-                  int n_out, int kdim, TOut* __restrict__ C) {
+                  int n_out, int kdim, TOut* __restrict__ C, T* __restrict__ pre) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs0[BK][BN + 4];
   __shared__ float Bs1[(EPI == EPI_SWIGLU) ? BK : 1][BN + 4];
@@ -101,13 +101,20 @@ grouped_gemm_simt(const T* __restrict__ A, const T* __restrict__ B0, const T* __
       const int n = n0 + tx * 4 + j;
       if (n >= n_out) continue;
       float v;
+      // pre (backward pass): [row][2 * n_out], gate | up pre-activations (GELU: z)
+      T* pre_row = pre ? pre + static_cast<size_t>(row0 + r) * 2 * n_out : nullptr;
       if (EPI == EPI_SWIGLU) {
         const float g = acc0[i][j];
         v = g / (1.f + expf(-g)) * acc1[i][j];
+        if (pre_row) {
+          pre_row[n] = from_f32<T>(g);
+          pre_row[n_out + n] = from_f32<T>(acc1[i][j]);
+        }
       } else if (EPI == EPI_GELU) {
         float z = acc0[i][j];
         if (bias) z += to_f32(bias[static_cast<size_t>(e) * n_out + n]);
         v = 0.5f * z * (1.f + erff(z * 0.70710678118654752f));
+        if (pre_row) pre_row[n] = from_f32<T>(z);
       } else {
         v = acc0[i][j];
         if (bias) v += to_f32(bias[static_cast<size_t>(e) * n_out + n]);
@@ -119,7 +126,7 @@ grouped_gemm_simt(const T* __restrict__ A, const T* __restrict__ B0, const T* __
 
 template <typename T>
 moe_status run(const moe_config& c, int64_t a_max, const T* x_perm, const int32_t* offsets,
-               const moe_expert_weights& w, T* h, float* o, cudaStream_t s, int part) {
+               const moe_expert_weights& w, T* h, float* o, T* pre, cudaStream_t s, int part) {
   const int N = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
   const int64_t mtiles = N + (a_max + BM - 1) / BM;  // upper bound on (expert, m-tile) pairs
   if (mtiles > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
@@ -130,17 +137,17 @@ moe_status run(const moe_config& c, int64_t a_max, const T* x_perm, const int32_
     if (swiglu)
       grouped_gemm_simt<T, EPI_SWIGLU, T><<<g1, kThreads, 0, s>>>(
           x_perm, static_cast<const T*>(w.w_gate), static_cast<const T*>(w.w_up), nullptr,
-          offsets, N, F, d, h);
+          offsets, N, F, d, h, pre);
     else
       grouped_gemm_simt<T, EPI_GELU, T><<<g1, kThreads, 0, s>>>(
           x_perm, static_cast<const T*>(w.w1), nullptr, static_cast<const T*>(w.b1), offsets, N,
-          F, d, h);
+          F, d, h, pre);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (part & 2) {
     grouped_gemm_simt<T, EPI_LINEAR, float><<<g2, kThreads, 0, s>>>(
         h, static_cast<const T*>(swiglu ? w.w_down : w.w2), nullptr,
-        swiglu ? nullptr : static_cast<const T*>(w.b2), offsets, N, d, F, o);
+        swiglu ? nullptr : static_cast<const T*>(w.b2), offsets, N, d, F, o, nullptr);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
@@ -150,13 +157,14 @@ moe_status run(const moe_config& c, int64_t a_max, const T* x_perm, const int32_
 
 moe_status launch_ffn_simt(const moe_config& c, int64_t a_max, const void* x_perm,
                            const int32_t* offsets, const moe_expert_weights& w, void* h, float* o,
-                           cudaStream_t s, int part) {
+                           void* pre, cudaStream_t s, int part) {
   if (a_max == 0) return MOE_OK;
   if (c.dtype == MOE_BF16)
     return run<__nv_bfloat16>(c, a_max, static_cast<const __nv_bfloat16*>(x_perm), offsets, w,
-                              static_cast<__nv_bfloat16*>(h), o, s, part);
+                              static_cast<__nv_bfloat16*>(h), o,
+                              static_cast<__nv_bfloat16*>(pre), s, part);
   return run<float>(c, a_max, static_cast<const float*>(x_perm), offsets, w,
-                    static_cast<float*>(h), o, s, part);
+                    static_cast<float*>(h), o, static_cast<float*>(pre), s, part);
 }
 
 }  // namespace moe

@@ -77,7 +77,29 @@ struct TcArgs {
   void* out;               // h (bf16, row length F) or o (fp32, row length d)
   int ldo;
   uint32_t* status;
+  void* pre;               // gate/up: NULL, or [rows][2F] bf16 pre-activations
+                           // (gate | up) kept for the backward pass
 };
+
+// The 32 gate and 32 up pre-activations of one row chunk, rounded to bf16, at
+// dst[0..32) and dst[F..F+32) (the backward pass's copy).
+__device__ __forceinline__ void store_pre(__nv_bfloat16* dst, int F, const uint32_t (&g)[32],
+                                          const uint32_t (&u)[32]) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t(&src)[32] = half == 0 ? g : u;
+    uint32_t p[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(src[2 * j]),
+                                               __uint_as_float(src[2 * j + 1]));
+      p[j] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(dst + half * F);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) d4[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+  }
+}
 
 // MODE 0: gate/up + SwiGLU -> h (bf16). MODE 1: down -> o (fp32).
 template <int MODE, int BNH>
@@ -318,6 +340,10 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             for (int v = 0; v < 4; ++v)
               dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
                                   packed[4 * v + 3]);
+            if (args.pre != nullptr)
+              store_pre(static_cast<__nv_bfloat16*>(args.pre) + grow * 2 * args.ldo +
+                            n * Sh::OUT_COLS + c * 32,
+                        args.ldo, g, u);
           }
         }
       } else {
@@ -610,6 +636,10 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
             for (int v = 0; v < 4; ++v)
               dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
                                   packed[4 * v + 3]);
+            if (args.pre != nullptr)
+              store_pre(static_cast<__nv_bfloat16*>(args.pre) + grow * 2 * args.ldo + n * 128 +
+                            c * 32,
+                        args.ldo, g, u);
           }
         }
       } else {
@@ -742,7 +772,7 @@ bool ffn_tc_supported(const moe_config& c) {
 
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w, void* h, float* o,
-                         uint32_t* status, cudaStream_t s, int part) {
+                         void* pre, uint32_t* status, cudaStream_t s, int part) {
   if (rows == 0) return MOE_OK;
   const int E = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
   const bool pairs1 = use_pairs(c, rows, d);  // gate/up: reduction over d
@@ -757,7 +787,7 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
         !make_map(&mg, w.w_gate, static_cast<uint64_t>(E) * F, d, 128) ||
         !make_map(&mu, w.w_up, static_cast<uint64_t>(E) * F, d, 128))
       return MOE_ERR_CUDA;
-    TcArgs a1{offsets, E, d, F / 128, F, h, F, status};
+    TcArgs a1{offsets, E, d, F / 128, F, h, F, status, pre};
     if (pairs1) {
       if (launch_pair<0>(mx, mg, mu, a1, ptiles * (F / 128), s) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -777,7 +807,7 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
     if (!make_map(&mh, h, rows, F, 128) ||
         !make_map(&md, w.w_down, static_cast<uint64_t>(E) * d, F, pairs2 ? 128 : 256))
       return MOE_ERR_CUDA;
-    TcArgs a2{offsets, E, F, d / 256, d, o, d, status};
+    TcArgs a2{offsets, E, F, d / 256, d, o, d, status, nullptr};
     if (pairs2) {
       if (launch_pair<1>(mh, md, md, a2, ptiles * (d / 256), s) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -5,6 +5,8 @@
 
 #include <math.h>
 
+#include <algorithm>
+
 #include <mutex>
 
 namespace moe {
@@ -32,6 +34,7 @@ bool config_valid(const moe_config* c, moe_status* why) {
   if (c->gate_mode != MOE_GATE_RENORM && c->gate_mode != MOE_GATE_SOFTMAX)
     return bad(MOE_ERR_INVALID);
   if (c->n_shared < 0) return bad(MOE_ERR_INVALID);
+  if (c->save_for_backward != 0 && c->save_for_backward != 1) return bad(MOE_ERR_INVALID);
   if (c->n_shared > 8) return bad(MOE_ERR_UNSUPPORTED);
   if (c->T < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0)
     return bad(MOE_ERR_INVALID);
@@ -99,6 +102,16 @@ WsLayout ws_layout(const moe_config* c) {
   L.x_perm = take(A * d * es);
   L.h = take(A * F * es);
   L.o = take(A * d * 4);
+  const bool bw = c->save_for_backward != 0;
+  // router-gradient K splits: about 1024 tokens each, at most 32
+  L.rsplits = bw ? static_cast<int>(std::min<size_t>(32, std::max<size_t>(1, T / 1024))) : 0;
+  L.logits = take(bw ? T * N * 4 : 0);
+  L.pre = take(bw ? A * 2 * F * es : 0);
+  L.count = take(bw ? N * 4 : 0);
+  L.dout = take(bw ? A * d * es : 0);
+  L.dg = take(bw ? T * K * 4 : 0);
+  L.dl = take(bw ? T * N * 4 : 0);
+  L.rpart = take(bw ? static_cast<size_t>(L.rsplits) * N * (d + 1) * 4 : 0);
   L.total = total;
   return L;
 }
@@ -128,11 +141,12 @@ uint8_t* at(void* ws, size_t off) {
   return static_cast<uint8_t*>(ws) + off;
 }
 
-RouterScratch router_scratch(void* ws, const WsLayout& L) {
+RouterScratch router_scratch(void* ws, const WsLayout& L, bool keep_logits) {
   return RouterScratch{reinterpret_cast<float*>(at(ws, L.psum)),
                        reinterpret_cast<int32_t*>(at(ws, L.pcnt)),
                        reinterpret_cast<__nv_bfloat16*>(at(ws, L.w3)),
-                       reinterpret_cast<float*>(at(ws, L.part))};
+                       reinterpret_cast<float*>(at(ws, L.part)),
+                       keep_logits ? reinterpret_cast<float*>(at(ws, L.logits)) : nullptr};
 }
 
 moe_status check_weights(const moe_config* c, const moe_expert_weights* w) {
@@ -161,15 +175,17 @@ void trace(int i, cudaStream_t s) {
 
 moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offsets,
                     const moe_expert_weights* w, float* o, moe_stats* stats, void* ws,
-                    cudaStream_t s, bool traced) {
+                    cudaStream_t s, bool traced, bool keep_pre) {
   const WsLayout L = ws_layout(c);
   void* h = at(ws, L.h);
+  void* pre = keep_pre ? at(ws, L.pre) : nullptr;
   const bool tc = ffn_tc_supported(*c);
   uint32_t* status = stats ? stats->status : nullptr;
   for (int part = 1; part <= 2; ++part) {
     const int64_t rows = rows_max_of(c);
-    const moe_status r = tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, status, s, part)
-                            : launch_ffn_simt(*c, rows, x_perm, offsets, *w, h, o, s, part);
+    const moe_status r =
+        tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, pre, status, s, part)
+           : launch_ffn_simt(*c, rows, x_perm, offsets, *w, h, o, pre, s, part);
     if (r != MOE_OK) return r;
     if (traced) trace(2 + part, s);
   }
@@ -204,6 +220,11 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   const int ffn = 2;                                    // gate/up, down
   const int combine = 1;
   return router + stats + dispatch + ffn + combine;
+}
+
+int32_t moe_backward_launch_count(const moe_config* cfg) {
+  if (!config_valid(cfg, nullptr) || cfg->save_for_backward == 0) return -1;
+  return backward_launch_count(*cfg);
 }
 
 int32_t moe_ffn_uses_tensor_cores(const moe_config* cfg) {
@@ -244,7 +265,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r, con
       return MOE_ERR_INVALID;
     if (moe_status s = check_ws(cfg, ws)) return s;
     const WsLayout L = ws_layout(cfg);
-    return launch_router(*cfg, x, w_r, b_r, idx, gate, router_scratch(ws, L), stats,
+    return launch_router(*cfg, x, w_r, b_r, idx, gate, router_scratch(ws, L, false), stats,
                          static_cast<cudaStream_t>(stream));
   } catch (...) {
     return MOE_ERR_CUDA;
@@ -283,7 +304,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
     if (moe_status s = check_weights(cfg, weights)) return s;
     if (moe_status s = check_ws(cfg, ws)) return s;
     return ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws,
-                    static_cast<cudaStream_t>(stream), false);
+                    static_cast<cudaStream_t>(stream), false, false);
   } catch (...) {
     return MOE_ERR_CUDA;
   }
@@ -310,7 +331,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r, c
   try {
     moe_status why = MOE_OK;
     if (!config_valid(cfg, &why)) return why;
-    if (!x || !w_r || !y) return MOE_ERR_INVALID;
+    // no token: x and y may be NULL (an empty tensor has no storage)
+    if (!w_r || (cfg->T > 0 && (!x || !y))) return MOE_ERR_INVALID;
     if (!aligned16(x) || !aligned16(w_r) || !aligned16(y) || (b_r && !aligned16(b_r)))
       return MOE_ERR_INVALID;
     if (moe_status s = check_weights(cfg, weights)) return s;
@@ -324,20 +346,60 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r, c
     int32_t* tos = reinterpret_cast<int32_t*>(at(ws, L.token_of_slot));
     void* x_perm = at(ws, L.x_perm);
     float* o = reinterpret_cast<float*>(at(ws, L.o));
+    const bool keep = cfg->save_for_backward != 0;
     trace(0, s);
-    moe_status r = launch_router(*cfg, x, w_r, b_r, idx, gate, router_scratch(ws, L), stats, s);
+    moe_status r =
+        launch_router(*cfg, x, w_r, b_r, idx, gate, router_scratch(ws, L, keep), stats, s);
     if (r != MOE_OK) return r;
     trace(1, s);
+    // the backward pass reads the counts from the workspace (the router's
+    // statistics kernel still writes the caller's copy)
+    moe_stats dst = stats ? *stats : moe_stats{};
+    if (keep) dst.count = reinterpret_cast<int32_t*>(at(ws, L.count));
+    const bool any = dst.count || dst.kept || dst.n_dropped || dst.status;
     r = launch_dispatch(*cfg, x, idx, offsets, slot_of, tos, x_perm,
                         reinterpret_cast<int32_t*>(at(ws, L.ghist)),
-                        reinterpret_cast<int32_t*>(at(ws, L.gbase)), stats, s);
+                        reinterpret_cast<int32_t*>(at(ws, L.gbase)), any ? &dst : nullptr, s);
     if (r != MOE_OK) return r;
     trace(2, s);
-    r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true);
+    r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true, keep);
     if (r != MOE_OK) return r;
     r = launch_combine(*cfg, o, slot_of, gate, x, y, s);
     trace(5, s);
     return r;
+  } catch (...) {
+    return MOE_ERR_CUDA;
+  }
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* w_r,
+                        const moe_expert_weights* weights, const void* dy, float z_coef,
+                        moe_grads* grads, moe_stats* stats, void* ws, moe_stream_t stream) {
+  try {
+    moe_status why = MOE_OK;
+    if (!config_valid(cfg, &why)) return why;
+    if (cfg->save_for_backward == 0) return MOE_ERR_INVALID;
+    const bool none = cfg->T == 0;  // no token: x, dy and dx may be NULL
+    if (!w_r || !grads || !grads->dw_r || (!none && (!x || !dy || !grads->dx)))
+      return MOE_ERR_INVALID;
+    if (!isfinite(z_coef) || z_coef < 0.f) return MOE_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w_r) || !aligned16(dy) || !aligned16(grads->dx) ||
+        !aligned16(grads->dw_r) || (grads->db_r && !aligned16(grads->db_r)))
+      return MOE_ERR_INVALID;
+    if (moe_status s = check_weights(cfg, weights)) return s;
+    if (cfg->activation == MOE_SWIGLU) {
+      if (!grads->dw_gate || !grads->dw_up || !grads->dw_down) return MOE_ERR_INVALID;
+      if (!aligned16(grads->dw_gate) || !aligned16(grads->dw_up) || !aligned16(grads->dw_down))
+        return MOE_ERR_INVALID;
+    } else {
+      if (!grads->dw1 || !grads->dw2) return MOE_ERR_INVALID;
+      if (cfg->has_bias && (!grads->db1 || !grads->db2)) return MOE_ERR_INVALID;
+      if (!aligned16(grads->dw1) || !aligned16(grads->dw2)) return MOE_ERR_INVALID;
+    }
+    if (moe_status s = check_ws(cfg, ws)) return s;
+    const WsLayout L = ws_layout(cfg);
+    return launch_backward(*cfg, L, ws, x, w_r, *weights, dy, z_coef, *grads,
+                           stats ? stats->status : nullptr, static_cast<cudaStream_t>(stream));
   } catch (...) {
     return MOE_ERR_CUDA;
   }

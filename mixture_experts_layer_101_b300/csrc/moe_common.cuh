@@ -64,10 +64,21 @@ struct WsLayout {
   size_t token_of_slot;       // [A_max] (moe_forward only)
   size_t x_perm;              // [A_max][d] dtype (moe_forward only)
   size_t h;                   // [A_max][F] dtype
-  size_t o;                   // [A_max][d] fp32 (moe_forward only)
+  size_t o;                   // [A_max][d] fp32 (moe_forward only); the backward
+                              // pass reuses it for the expert input gradients
+  // save_for_backward only (size 0 otherwise):
+  size_t logits;              // [T][N] fp32 router logits
+  size_t pre;                 // [R_max][2F] dtype: SwiGLU gate | up pre-activations
+                              // (GELU: z in the first F columns); the backward pass
+                              // overwrites them in place with their gradients
+  size_t count;               // [N] int32 assignments per expert
+  size_t dout;                // [R_max][d] dtype: expert output gradients
+  size_t dg;                  // [T][K] fp32 gate gradients
+  size_t dl;                  // [T][N] fp32 logit gradients
+  size_t rpart;               // [rsplits][N][d + 1] fp32 router-gradient partials
   size_t total;
   int64_t a_max;
-  int nblk_r, nblk_d;
+  int nblk_r, nblk_d, rsplits;
 };
 
 // Host-side helpers implemented in moe_api.cu.
@@ -91,12 +102,14 @@ struct RouterTcPlan {
 RouterTcPlan router_tc_plan(const moe_config& c);
 
 // Router scratch: per-block partial statistics (always), plus the weight
-// split and partial logits of the tensor-core router (NULL: CUDA-core router).
+// split and partial logits of the tensor-core router (NULL: CUDA-core router)
+// and the [T][N] logits kept for the backward pass (NULL: not kept).
 struct RouterScratch {
   float* psum;
   int32_t* pcnt;
   __nv_bfloat16* w3;
   float* part;
+  float* logits;
 };
 moe_status launch_router(const moe_config& c, const void* x, const float* w_r,
                          const float* b_r, int32_t* idx, float* gate, const RouterScratch& sc,
@@ -104,7 +117,7 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r,
 moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const void* x,
                             const float* w_r, const float* b_r, int32_t* idx, float* gate,
                             __nv_bfloat16* w3, float* part, float* psum, int32_t* pcnt,
-                            uint32_t* status, cudaStream_t s);
+                            uint32_t* status, float* logits, cudaStream_t s);
 
 moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* offsets, int32_t* slot_of, int32_t* token_of_slot,
@@ -116,15 +129,24 @@ moe_status launch_combine(const moe_config& c, const float* o, const int32_t* sl
 
 // Expert FFN on CUDA cores (any dtype/shape) over the N + n_shared experts;
 // rows = rows of x_perm / h / o. part: 1 = gate/up (or the first Linear +
-// GELU) into h, 2 = down projection into o, 3 = both.
+// GELU) into h, 2 = down projection into o, 3 = both. pre (NULL or
+// [rows][2F] dtype): the pre-activations kept for the backward pass.
 moe_status launch_ffn_simt(const moe_config& c, int64_t rows, const void* x_perm,
                            const int32_t* offsets, const moe_expert_weights& w,
-                           void* h, float* o, cudaStream_t s, int part);
+                           void* h, float* o, void* pre, cudaStream_t s, int part);
 
 // Expert FFN on tcgen05 tensor cores (bf16, d % 256 == 0, F % 128 == 0).
 bool ffn_tc_supported(const moe_config& c);
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w,
-                         void* h, float* o, uint32_t* status, cudaStream_t s, int part);
+                         void* h, float* o, void* pre, uint32_t* status, cudaStream_t s,
+                         int part);
+
+// Backward pass (backward.cu): every gradient, from the state moe_forward
+// kept in the workspace.
+moe_status launch_backward(const moe_config& c, const WsLayout& L, void* ws, const void* x,
+                           const float* w_r, const moe_expert_weights& w, const void* dy,
+                           float z_coef, const moe_grads& g, uint32_t* status, cudaStream_t s);
+int backward_launch_count(const moe_config& c);
 
 }  // namespace moe

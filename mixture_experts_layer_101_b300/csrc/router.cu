@@ -39,7 +39,7 @@ router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
               int T, int d, int N, int K,
               int32_t* __restrict__ idx_out, float* __restrict__ gate_out,
               float* __restrict__ psum, int32_t* __restrict__ pcnt,
-              uint32_t* __restrict__ status) {
+              uint32_t* __restrict__ status, float* __restrict__ logits_out) {
   constexpr int WS_K = kWarps / WS_N;
   constexpr int NP = NPW * WS_N;                  // padded expert count
   constexpr int LT = (NPW == 8) ? 32 : 8;         // lanes across tokens
@@ -138,7 +138,7 @@ router_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
       v[j] = (e < N) ? red[tl * NP + e] : -INFINITY;
     }
     route_one_token<NJ>(v, N, K, static_cast<size_t>(t), lane, sel_bias, gate_mode, idx_out,
-                        gate_out, pacc, zacc, hacc, scnt, status);
+                        gate_out, pacc, zacc, hacc, scnt, status, logits_out);
   }
 
   // ---- phase D: per-block partials in a fixed order ----
@@ -218,14 +218,14 @@ __global__ void route_laux_kernel(const float* __restrict__ psum, const int32_t*
 template <typename Tx>
 cudaError_t launch_router_t(const moe_config& c, const Tx* x, const float* w_r, const float* b_r,
                             int32_t* idx, float* gate, float* psum, int32_t* pcnt,
-                            uint32_t* status, cudaStream_t s) {
+                            uint32_t* status, float* logits, cudaStream_t s) {
   const int nblk = (c.T + BM - 1) / BM;
   const int N = c.n_experts;
   dim3 grid(nblk), block(kThreads);
 #define MOE_ROUTER(NPW, WSN)                                                                  \
   router_kernel<Tx, NPW, WSN><<<grid, block, 0, s>>>(x, w_r, b_r, c.select_bias, c.gate_mode, \
                                                      c.T, c.d_model, N, c.top_k, idx, gate,    \
-                                                     psum, pcnt, status)
+                                                     psum, pcnt, status, logits)
   if (N <= 8) MOE_ROUTER(8, 1);
   else if (N <= 32) MOE_ROUTER(32, 1);
   else if (N <= 64) MOE_ROUTER(32, 2);
@@ -249,16 +249,16 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
   if (plan.use && sc.w3 != nullptr && (plan.fused || sc.part != nullptr)) {
     nblk = plan.stat_blocks;
     const moe_status r = launch_router_tc(c, plan, x, w_r, b_r, idx, gate, sc.w3, sc.part, psum,
-                                          pcnt, status, s);
+                                          pcnt, status, sc.logits, s);
     if (r != MOE_OK) return r;
   } else {
     cudaError_t err;
     if (c.dtype == MOE_BF16)
       err = launch_router_t(c, static_cast<const __nv_bfloat16*>(x), w_r, b_r, idx, gate, psum,
-                            pcnt, status, s);
+                            pcnt, status, sc.logits, s);
     else
       err = launch_router_t(c, static_cast<const float*>(x), w_r, b_r, idx, gate, psum, pcnt,
-                            status, s);
+                            status, sc.logits, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (st && (st->count || st->f || st->P || st->l_aux || st->z_loss || st->entropy)) {
@@ -348,7 +348,7 @@ extern "C" moe_status moe_route_no_workspace(const moe_config* cfg, const void* 
     float* psum = static_cast<float*>(scratch);
     int32_t* pcnt = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(scratch) +
                                                kRouteScratchElems * sizeof(float));
-    const RouterScratch sc{psum, pcnt, nullptr, nullptr};  // CUDA-core router
+    const RouterScratch sc{psum, pcnt, nullptr, nullptr, nullptr};  // CUDA-core router
     return launch_router(*cfg, x, w_r, b_r, idx, gate, sc, stats,
                          static_cast<cudaStream_t>(stream));
   } catch (...) {

@@ -22,14 +22,20 @@ constexpr int kSelectWarps = 8;  // warps per router block (256 threads)
 // lane 0 adds the token's squared log-sum-exp to zacc and its routing entropy
 // to hacc. sel_bias (NULL or [N]) shifts the logits for the top-K choice
 // only ("混合专家模型（Mixture of Experts, MoE）" 结构 4); gate_mode picks the
-// renormalised or the full-softmax gate.
+// renormalised or the full-softmax gate. logits_out (NULL or [T][N]) keeps
+// the token's logits for the backward pass.
 template <int NJ>
 __device__ __forceinline__ void route_one_token(const float (&v)[NJ], int N, int K, size_t t,
                                                 int lane, const float* __restrict__ sel_bias,
                                                 int gate_mode, int32_t* __restrict__ idx_out,
                                                 float* __restrict__ gate_out, float (&pacc)[NJ],
                                                 float& zacc, float& hacc, int32_t* scnt,
-                                                uint32_t* status) {
+                                                uint32_t* status, float* logits_out = nullptr) {
+  if (logits_out != nullptr) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if (lane + 32 * j < N) logits_out[t * N + lane + 32 * j] = v[j];
+  }
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < NJ; ++j)

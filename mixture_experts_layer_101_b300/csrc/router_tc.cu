@@ -93,6 +93,7 @@ struct GemmArgs {
   float* gate;
   float* psum;   // [N+2][nblk], nblk = ceil(T/128)
   int32_t* pcnt; // [N][nblk]
+  float* logits; // [T][N] kept for the backward pass, or NULL
 };
 
 // ---- fused selection in the GEMM epilogue ----------------------------------
@@ -143,6 +144,12 @@ __device__ __forceinline__ void fused_select(float (&v)[NPT], const GemmArgs& a,
     }
   }
   if (bad) set_status(a.status, MOE_ERR_NONFINITE);
+  if (a.logits != nullptr) {
+    float* lrow = a.logits + static_cast<size_t>(t) * N;
+#pragma unroll
+    for (int e = 0; e < NPT; ++e)
+      if (e < N) lrow[e] = v[e];
+  }
   // top-K
   uint32_t taken[(NPT + 31) / 32];
 #pragma unroll
@@ -436,9 +443,10 @@ router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 template <int NJ>
 __global__ void __launch_bounds__(256)
 router_topk_kernel(const float* __restrict__ part, int S, int NP, const float* __restrict__ b_r,
-                   const float* __restrict__ sel_bias, int gate_mode, int T, int N, int K, int32_t* __restrict__ idx_out,
-                   float* __restrict__ gate_out, float* __restrict__ psum,
-                   int32_t* __restrict__ pcnt, uint32_t* __restrict__ status) {
+                   const float* __restrict__ sel_bias, int gate_mode, int T, int N, int K,
+                   int32_t* __restrict__ idx_out, float* __restrict__ gate_out,
+                   float* __restrict__ psum, int32_t* __restrict__ pcnt,
+                   uint32_t* __restrict__ status, float* __restrict__ logits_out) {
   __shared__ float pw[kSelectWarps][256];
   __shared__ float zh[2 * kSelectWarps];
   __shared__ int32_t scnt[256];
@@ -467,7 +475,7 @@ router_topk_kernel(const float* __restrict__ part, int S, int NP, const float* _
       v[j] = acc;
     }
     route_one_token<NJ>(v, N, K, static_cast<size_t>(t), lane, sel_bias, gate_mode, idx_out,
-                        gate_out, pacc, zacc, hacc, scnt, status);
+                        gate_out, pacc, zacc, hacc, scnt, status, logits_out);
   }
   write_block_stats<NJ>(pacc, zacc, hacc, pw, zh, scnt, N, blockIdx.x, psum, pcnt);
 }
@@ -545,7 +553,7 @@ RouterTcPlan router_tc_plan(const moe_config& c) {
 moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const void* x,
                             const float* w_r, const float* b_r, int32_t* idx, float* gate,
                             __nv_bfloat16* w3, float* part, float* psum, int32_t* pcnt,
-                            uint32_t* status, cudaStream_t s) {
+                            uint32_t* status, float* logits, cudaStream_t s) {
   const int N = c.n_experts, d = c.d_model, T = c.T;
   router_split_kernel<<<sm_count() * 4, 256, 0, s>>>(w_r, N, p.NP, d, w3);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
@@ -554,7 +562,7 @@ moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const vo
       !make_map(&mw, w3, static_cast<uint64_t>(3) * p.NP, d, p.NPT))
     return MOE_ERR_CUDA;
   GemmArgs a{T, p.NP, d / BK, p.kb_per_split, part, status, N, c.top_k, c.gate_mode, b_r,
-             c.select_bias, idx, gate, psum, pcnt};
+             c.select_bias, idx, gate, psum, pcnt, logits};
   const dim3 grid((T + BM - 1) / BM, p.NP / p.NPT, p.S);
   cudaError_t e;
   if (p.fused) {
@@ -568,18 +576,15 @@ moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const vo
   else e = launch_gemm<32, false>(mx, mw, a, grid, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
-  if (N <= 32)
-    router_topk_kernel<1><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, T, N, c.top_k, idx, gate,
-                                               psum, pcnt, status);
-  else if (N <= 64)
-    router_topk_kernel<2><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, T, N, c.top_k, idx, gate,
-                                               psum, pcnt, status);
-  else if (N <= 128)
-    router_topk_kernel<4><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, T, N, c.top_k, idx, gate,
-                                               psum, pcnt, status);
-  else
-    router_topk_kernel<8><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, T, N, c.top_k, idx, gate,
-                                               psum, pcnt, status);
+#define MOE_TOPK(NJ)                                                                           \
+  router_topk_kernel<NJ><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, \
+                                              T, N, c.top_k, idx, gate, psum, pcnt, status,    \
+                                              logits)
+  if (N <= 32) MOE_TOPK(1);
+  else if (N <= 64) MOE_TOPK(2);
+  else if (N <= 128) MOE_TOPK(4);
+  else MOE_TOPK(8);
+#undef MOE_TOPK
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -29,7 +29,8 @@ MOE_GATE_RENORM, MOE_GATE_SOFTMAX = 0, 1
 EXPORTED = ["moe_workspace_size", "moe_capacity", "moe_route", "moe_route_no_workspace",
             "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_status_string",
-            "moe_trace_events", "moe_selftest_bounded_wait", "moe_forward_launch_count",
+            "moe_backward", "moe_trace_events", "moe_selftest_bounded_wait",
+            "moe_forward_launch_count", "moe_backward_launch_count",
             "moe_ffn_uses_tensor_cores"]
 
 
@@ -46,7 +47,7 @@ class MoEConfig(ctypes.Structure):
                 ("has_bias", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
                 ("alpha", ctypes.c_float), ("add_residual", ctypes.c_int32),
                 ("gate_mode", ctypes.c_int32), ("select_bias", ctypes.c_void_p),
-                ("n_shared", ctypes.c_int32)]
+                ("n_shared", ctypes.c_int32), ("save_for_backward", ctypes.c_int32)]
 
 
 class MoEStatsC(ctypes.Structure):
@@ -60,6 +61,11 @@ class MoEExpertWeightsC(ctypes.Structure):
     _fields_ = [("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
                 ("w_down", ctypes.c_void_p), ("w1", ctypes.c_void_p), ("b1", ctypes.c_void_p),
                 ("w2", ctypes.c_void_p), ("b2", ctypes.c_void_p)]
+
+
+class MoEGradsC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dx", "dw_r", "db_r", "dw_gate", "dw_up",
+                                               "dw_down", "dw1", "db1", "dw2", "db2")]
 
 
 _lib = None
@@ -97,9 +103,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_expert_ffn.argtypes = [cfgp, P, P, wp, P, statp, P, P]
     lib.moe_combine.argtypes = [cfgp, P, P, P, P, P, P]
     lib.moe_forward.argtypes = [cfgp, P, P, P, wp, P, statp, P, P]
+    lib.moe_backward.argtypes = [cfgp, P, P, wp, P, ctypes.c_float,
+                                 ctypes.POINTER(MoEGradsC), statp, P, P]
+    lib.moe_backward_launch_count.argtypes = [cfgp]
+    lib.moe_backward_launch_count.restype = ctypes.c_int32
     lib.moe_trace_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
     lib.moe_trace_events.restype = ctypes.c_int
-    for name in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward"):
+    for name in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
+                 "moe_backward"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -131,6 +142,7 @@ class LayerConfig:
     gate_mode: str = "renorm"          # "renorm" | "softmax"
     select_bias: torch.Tensor | None = None  # [N] fp32 CUDA tensor: top-K choice only
     n_shared: int = 0                  # shared experts after the N routed ones
+    save_for_backward: bool = False    # forward keeps what moe_backward needs
 
     @classmethod
     def from_workload(cls, w, T: int | None = None) -> "LayerConfig":
@@ -151,7 +163,8 @@ class LayerConfig:
                          int(self.has_bias), float(self.capacity_factor), float(self.alpha),
                          int(self.add_residual),
                          MOE_GATE_SOFTMAX if self.gate_mode == "softmax" else MOE_GATE_RENORM,
-                         _ptr(self.select_bias), int(self.n_shared))
+                         _ptr(self.select_bias), int(self.n_shared),
+                         int(self.save_for_backward))
 
 
 def _ptr(t) -> int | None:
@@ -233,6 +246,15 @@ def ffn_uses_tensor_cores(cfg: LayerConfig) -> bool:
 
 
 moe_ffn_uses_tensor_cores = ffn_uses_tensor_cores
+
+
+def backward_launch_count(cfg: LayerConfig) -> int:
+    """Kernels one moe_backward launches for cfg (db_r requested); -1 if cfg
+    does not save for backward."""
+    return int(load_library().moe_backward_launch_count(ctypes.byref(cfg.c())))
+
+
+moe_backward_launch_count = backward_launch_count
 
 
 def forward_launch_count(cfg: LayerConfig) -> int:
@@ -334,6 +356,38 @@ def moe_forward(cfg: LayerConfig, x, w_r, b_r, weights: dict, y, stats: Stats | 
     _check(code, "moe_forward")
 
 
+GRAD_NAMES = ("dx", "dw_r", "db_r", "dw_gate", "dw_up", "dw_down", "dw1", "db1", "dw2", "db2")
+
+
+def grads_c(grads: dict) -> MoEGradsC:
+    return MoEGradsC(*(_ptr(grads.get(n)) for n in GRAD_NAMES))
+
+
+def alloc_grads(cfg: LayerConfig, router_bias: bool = True, device="cuda") -> dict:
+    """fp32 gradient buffers shaped like the inputs and weights they belong to."""
+    T, d, F, N = cfg.T, cfg.d_model, cfg.d_ff, cfg.n_experts
+    E = N + cfg.n_shared
+    z = lambda *shape: torch.empty(shape, dtype=torch.float32, device=device)
+    g = {"dx": z(T, d), "dw_r": z(N, d), "db_r": z(N) if router_bias else None}
+    if cfg.activation == "swiglu":
+        g.update(dw_gate=z(E, F, d), dw_up=z(E, F, d), dw_down=z(E, d, F))
+    else:
+        g.update(dw1=z(E, F, d), dw2=z(E, d, F))
+        if cfg.has_bias:
+            g.update(db1=z(E, F), db2=z(E, d))
+    return g
+
+
+def moe_backward(cfg: LayerConfig, x, w_r, weights: dict, dy, z_coef: float, grads: dict,
+                 stats: Stats | None, ws, stream=None):
+    lib = load_library()
+    _check(lib.moe_backward(ctypes.byref(cfg.c()), _ptr(x), _ptr(w_r),
+                            ctypes.byref(weights_c(weights)), _ptr(dy), float(z_coef),
+                            ctypes.byref(grads_c(grads)),
+                            ctypes.byref(stats.c()) if stats else None, _ptr(ws),
+                            _stream(stream)), "moe_backward")
+
+
 def moe_trace_events(events):
     """Register up to 6 raw CUDA event handles (ints, e.g. TraceEvents.handles)
     that moe_forward records at its stage boundaries on this host thread;
@@ -407,7 +461,20 @@ class MoELayer:
     def forward(self, x, stream=None):
         moe_forward(self.cfg, x, self.w_r, self.b_r, self.weights, self.y, self.stats, self.ws,
                     stream)
+        self._x = x
         return self.y
+
+    def backward(self, dy, z_coef: float = 0.0, grads: dict | None = None, stream=None) -> dict:
+        """Gradients of <dy, y> + L_aux + z_coef * z_loss after forward() on a
+        config with save_for_backward (x must be unchanged since). Returns the
+        fp32 gradient tensors (allocated on first use unless given)."""
+        if grads is None:
+            if getattr(self, "_grads", None) is None:
+                self._grads = alloc_grads(self.cfg, self.b_r is not None, self.ws.device)
+            grads = self._grads
+        moe_backward(self.cfg, self._x, self.w_r, self.weights, dy, z_coef, grads, self.stats,
+                     self.ws, stream)
+        return grads
 
     def forward_host(self, x_host, y_host, x_dev, stream=None):
         """End-to-end call on host buffers: copy x (pinned host) in, run the

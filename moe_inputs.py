@@ -21,7 +21,8 @@ Workloads (shapes and distributions of the layers the MoE pages discuss):
                    SWITCH_SKEW_BIAS on experts 0..3 so that about 70% of the
                    tokens prefer those four experts.
 
-Seeds: x uses seed 0, expert e uses seed 1 + e, the router uses seed 1000.
+Seeds: x uses seed 0, expert e uses seed 1 + e, the router uses seed 1000,
+the output gradient dy of the backward pass seed 2000.
 Values are drawn in fp32 and then cast to the storage dtype. x and the router
 are always drawn on the CPU generator (so they are identical on every
 machine); expert weights are drawn on the device they are created on.
@@ -43,6 +44,7 @@ SWITCH_SKEW_EXPERTS = 4
 X_SEED = 0
 ROUTER_SEED = 1000
 SELECT_BIAS_SEED = 1001
+DY_SEED = 2000
 
 
 def expert_seed(e: int) -> int:
@@ -113,6 +115,14 @@ def make_x(w: MoEWorkload, T: int | None = None) -> torch.Tensor:
     """x [T][d] on the CPU, in the storage dtype."""
     T = w.T if T is None else T
     g = _gen(X_SEED, "cpu")
+    return torch.randn((T, w.d), generator=g, dtype=torch.float32).to(w.torch_dtype)
+
+
+def make_dy(w: MoEWorkload, T: int | None = None) -> torch.Tensor:
+    """Output gradient dy [T][d] for the backward pass on the CPU: N(0, 1) in
+    the storage dtype, seed 2000."""
+    T = w.T if T is None else T
+    g = _gen(DY_SEED, "cpu")
     return torch.randn((T, w.d), generator=g, dtype=torch.float32).to(w.torch_dtype)
 
 

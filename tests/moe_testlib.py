@@ -23,8 +23,10 @@ import torch
 import mixture_experts_layer_101_b300 as moe
 import moe_inputs
 from oracle import moe_oracle as O
+from oracle import moe_oracle_grad as OG
 
 NEAR_TIE_EPS = 1e-5
+BF16_U = 2.0 ** -8   # unit roundoff of bf16 round-to-nearest (8 significant bits)
 GATE_TOL = 1e-5
 STAT_RTOL = 1e-5
 
@@ -104,10 +106,11 @@ def check_routing(l64: np.ndarray, idx_gpu: np.ndarray, K: int):
 
 def bf16_rounding_bound(cfg: moe.LayerConfig, inp: dict, ref: dict) -> np.ndarray:
     """Per-element bound [len(tokens)][d] on |y_gpu - y| that bf16 storage
-    alone allows: h is rounded to bf16 once (relative error <= 2^-9 per
-    element, which reaches o as at most 2^-9 * sum_f |W_down[j, f]| |h_f|),
-    y is rounded to bf16 once (<= 2^-8 |y|, one ulp), plus 1e-3 * rms(y) for
-    fp32 accumulation order and gate rounding."""
+    alone allows, with the unit roundoff of bf16 round-to-nearest u = 2^-8
+    (8 significant bits): h is rounded to bf16 once (relative error <= u per
+    element, which reaches o as at most u * sum_f |W_down[j, f]| |h_f|), y is
+    rounded to bf16 once (<= u |y|), plus 1e-3 * rms(y) for fp32 accumulation
+    order and gate rounding."""
     x = O.f64(inp["x"])
     tok = ref["tokens"]
     bound = np.zeros((len(tok), cfg.d_model))
@@ -130,7 +133,7 @@ def bf16_rounding_bound(cfg: moe.LayerConfig, inp: dict, ref: dict) -> np.ndarra
             z = xe @ ew["w1"].T + (ew["b1"][None, :] if "b1" in ew else 0.0)
             h = O.gelu_erf(z)
             wd = ew["w2"]
-        scale = np.abs(h) @ np.abs(wd).T * 2.0 ** -9
+        scale = np.abs(h) @ np.abs(wd).T * BF16_U
         for r, (i, t, k) in enumerate(lst):
             bound[i] += (ref["gate"][t, k] if k >= 0 else 1.0) * scale[r]
     y = ref["y"]
@@ -196,3 +199,181 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
         assert err <= y_tolerance(cfg.dtype) * rms + 1e-30, (err, rms)
     return {"near_ties": n_near, "routing_diff": n_diff, "A": A, "y_err_over_rms":
             err / rms if rms > 0 else 0.0, "n_dropped": ref["n_dropped"]}
+
+
+# --------------------------------------------------------------- backward ----
+GRAD_TOL_F32 = 1e-4   # fp32 layers: max |err| <= 1e-4 * rms, as for y
+
+
+def _silu_parts(a):
+    s = 1.0 / (1.0 + np.exp(-a))
+    silu = a * s
+    d1 = s * (1.0 + a * (1.0 - s))
+    d2 = s * (1.0 - s) * (2.0 + a * (1.0 - 2.0 * s))
+    return silu, d1, d2
+
+
+def grad_rounding_bounds(cfg: moe.LayerConfig, inp: dict, dy, ref: dict) -> dict:
+    """First-order per-element bounds on |gradient_gpu - gradient| that the
+    bf16 roundings of a bf16 SwiGLU layer allow (u = 2^-8 per rounding):
+      do = g dy rounded (u |do|); the forward's h rounded (u |h|); the kept
+      pre-activations a, b rounded (u |a|, u |b|); the pre-activation
+      gradients da = dh b silu'(a), db = dh silu(a) rounded (u |da|, u |db|).
+    Propagated: E_dh = E_do |W_down|; E_da = u|da| + |b silu'(a)| E_dh +
+    |dh b silu''(a)| E_a + |dh silu'(a)| E_b; E_db = u|db| + |silu(a)| E_dh +
+    |dh silu'(a)| E_a; E_dW_down = E_do^T |h| + |do|^T E_h; E_dW_gate =
+    E_da^T |x|; E_dW_up = E_db^T |x|; E_dx_perm = E_da |W_gate| + E_db |W_up|;
+    through the gate gradient dg = <dy, o> with E_o = E_h |W_down|^T into the
+    logit gradient (renormalised gates: E_dl[i_k] = g_k (E_dg_k + sum g E_dg);
+    full-softmax gates: E_dl = p (E_dp + <p, E_dp>)), then E_dx += E_dl
+    |W_r| and E_dW_r = E_dl^T |x|. Each bound gets 1e-3 * rms of its
+    reference added for fp32 accumulation order and transcendental rounding.
+    Returns {"dx": [len(tokens)][d], "dw_r": [N][d], "db_r": [N],
+    "dw_gate": {e: [F][d]}, ...} for the tokens / experts in ref."""
+    u = BF16_U
+    K, N, S = cfg.top_k, cfg.n_experts, cfg.n_shared
+    fwd = ref["fwd"]
+    xs = O.f64(inp["x"])
+    dys = O.f64(dy)
+    T = xs.shape[0]
+    gate, idx, slot_of, p = fwd["gate"], fwd["idx"], fwd["slot_of"], fwd["p"]
+    reader = expert_reader(inp["experts"])
+    tok = ref["tokens"]
+    tok_pos = {int(t): i for i, t in enumerate(tok)}
+    E_dxp_tok = np.zeros((len(tok), xs.shape[1]))
+    E_dg = np.zeros((T, K))
+    bounds = {"dw_gate": {}, "dw_up": {}, "dw_down": {}}
+    rows_of = {}
+    for t in range(T):
+        for k in range(K):
+            if slot_of[t, k] >= 0:
+                rows_of.setdefault(int(idx[t, k]), []).append((t, k))
+    for s_ in range(S):
+        rows_of[N + s_] = [(t, -1) for t in range(T)]
+    for e, rows in rows_of.items():
+        ew = {kk: O.f64(v) for kk, v in reader(e).items() if v is not None}
+        ts = [t for t, _ in rows]
+        g = np.array([gate[t, k] if k >= 0 else 1.0 for t, k in rows])
+        xe = xs[ts]
+        a, b = xe @ ew["w_gate"].T, xe @ ew["w_up"].T
+        silu, d1, d2 = _silu_parts(a)
+        h = silu * b
+        do = g[:, None] * dys[ts]
+        dh = do @ ew["w_down"]
+        da, db = dh * b * d1, dh * silu
+        E_do, E_h, E_a, E_b = u * np.abs(do), u * np.abs(h), u * np.abs(a), u * np.abs(b)
+        E_dh = E_do @ np.abs(ew["w_down"])
+        E_da = (u * np.abs(da) + np.abs(b * d1) * E_dh + np.abs(dh * b * d2) * E_a +
+                np.abs(dh * d1) * E_b)
+        E_db = u * np.abs(db) + np.abs(silu) * E_dh + np.abs(dh * d1) * E_a
+        if e in ref["dw"]:
+            bounds["dw_down"][e] = E_do.T @ np.abs(h) + np.abs(do).T @ E_h
+            bounds["dw_gate"][e] = E_da.T @ np.abs(xe)
+            bounds["dw_up"][e] = E_db.T @ np.abs(xe)
+        E_dxp = E_da @ np.abs(ew["w_gate"]) + E_db @ np.abs(ew["w_up"])
+        E_o = E_h @ np.abs(ew["w_down"]).T
+        for r, (t, k) in enumerate(rows):
+            if t in tok_pos:
+                E_dxp_tok[tok_pos[t]] += E_dxp[r]
+            if k >= 0:
+                E_dg[t, k] = np.abs(dys[t]) @ E_o[r]
+    if cfg.gate_mode == "renorm":
+        sg = np.sum(gate * E_dg, axis=1, keepdims=True)
+        E_dl = np.zeros((T, N))
+        np.add.at(E_dl, (np.broadcast_to(np.arange(T)[:, None], idx.shape), idx),
+                  gate * (E_dg + sg))
+    else:
+        E_dp = np.zeros((T, N))
+        np.add.at(E_dp, (np.broadcast_to(np.arange(T)[:, None], idx.shape), idx), E_dg)
+        E_dl = p * (E_dp + np.sum(p * E_dp, axis=1, keepdims=True))
+    for e, dw in ref["dw"].items():  # experts without a kept row: exact zeros
+        for k, v in dw.items():
+            bounds.setdefault(k, {}).setdefault(e, np.zeros_like(v))
+    w_r = O.f64(inp["w_r"])
+    bounds["dx"] = E_dxp_tok + E_dl[tok] @ np.abs(w_r)
+    bounds["dw_r"] = E_dl.T @ np.abs(xs)
+    bounds["db_r"] = E_dl.sum(axis=0)
+    return bounds
+
+
+def run_backward(cfg: moe.LayerConfig, inp: dict, dy, z_coef: float):
+    """Forward (keeping state) then backward through the C ABI; returns the
+    host gradients, the GPU routing (from moe_route, the same kernels) and the
+    forward's y."""
+    cfg = moe.LayerConfig(**{**cfg.__dict__, "save_for_backward": True})
+    layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
+    y = layer.forward(inp["x"]).clone()
+    g = layer.backward(dy, z_coef)
+    torch.cuda.synchronize()
+    st = layer.stats.to_host()
+    T, K = cfg.T, cfg.top_k
+    idx = torch.zeros((T, K), dtype=torch.int32, device="cuda")
+    gate = torch.zeros((T, K), dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, inp["x"], inp["w_r"], inp["b_r"], idx, gate, None,
+                  moe.alloc_workspace(cfg))
+    torch.cuda.synchronize()
+    out = {k: (None if v is None else v.cpu()) for k, v in g.items()}
+    return out, idx.cpu().numpy().astype(np.int64), y.cpu(), st
+
+
+def compare(name: str, got, ref: np.ndarray, bound=None) -> float:
+    """bound None: max |err| <= GRAD_TOL_F32 * rms(ref); else elementwise
+    |err| <= bound + 1e-3 * rms(ref). Returns max |err| / rms(ref)."""
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    if ref.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = np.abs(got - ref)
+    emax = float(err.max())
+    if rms == 0.0:
+        assert emax == 0.0, (name, emax)
+        return 0.0
+    if bound is None:
+        assert emax <= GRAD_TOL_F32 * rms, (name, emax, rms, emax / rms)
+    else:
+        excess = err - (bound + 1e-3 * rms)
+        assert excess.max() <= 0.0, (name, emax, rms, float(excess.max()))
+    return emax / rms
+
+
+def check_backward(cfg: moe.LayerConfig, inp: dict, dy, z_coef: float, *, tokens=None,
+                   experts=None, router_grads: bool = True) -> dict:
+    """GPU gradients against the float64 backward oracle on the GPU's routing
+    (checked first, as in the forward tests). tokens / experts: the dx rows
+    and expert weight gradients compared (None = all). fp32 layers: max |err|
+    <= 1e-4 rms; bf16 (SwiGLU) layers: the per-element rounding bound of
+    grad_rounding_bounds. Returns the ratios max |err| / rms per gradient."""
+    grads, idx, _, st = run_backward(cfg, inp, dy, z_coef)
+    assert st["status"] == 0
+    K = cfg.top_k
+    x, w_r = inp["x"].cpu(), inp["w_r"].cpu()
+    b_r = None if inp["b_r"] is None else inp["b_r"].cpu()
+    sb = None if cfg.select_bias is None else cfg.select_bias.cpu()
+    l64 = O.router_logits(x, w_r, b_r)
+    key64 = l64 if sb is None else l64 + O.f64(sb)[None, :]
+    check_routing(key64, idx, K)
+    ref = OG.moe_backward(x, w_r, b_r, expert_reader(inp["experts"]), dy.cpu(), K=K,
+                          activation=cfg.activation, capacity_factor=cfg.capacity_factor,
+                          alpha=cfg.alpha, z_coef=z_coef, add_residual=cfg.add_residual,
+                          gate_mode=cfg.gate_mode, select_bias=sb, n_shared=cfg.n_shared,
+                          idx_override=idx, tokens=tokens, experts=experts,
+                          router_grads=router_grads)
+    bnd = None
+    if cfg.dtype == "bf16":
+        assert cfg.activation == "swiglu"
+        bnd = grad_rounding_bounds(cfg, inp, dy.cpu(), ref)
+    pick = (lambda k, e=None: None) if bnd is None else (
+        lambda k, e=None: bnd[k] if e is None else bnd[k][e])
+    ratios = {}
+    tok = ref["tokens"]
+    ratios["dx"] = compare("dx", grads["dx"].numpy()[tok], ref["dx"], pick("dx"))
+    if router_grads:
+        ratios["dw_r"] = compare("dw_r", grads["dw_r"].numpy(), ref["dw_r"], pick("dw_r"))
+        if b_r is not None:
+            ratios["db_r"] = compare("db_r", grads["db_r"].numpy(), ref["db_r"], pick("db_r"))
+    for e, dw in ref["dw"].items():
+        for k, v in dw.items():
+            r = compare(f"{k}[{e}]", grads[k].numpy()[e], v, pick(k, e))
+            ratios[k] = max(ratios.get(k, 0.0), r)
+    return ratios
