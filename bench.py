@@ -23,6 +23,11 @@ the layer, y and L_aux copied out, per step, wall clock with a sync per step.
 --impl reference: the float64 CPU oracle, unchanged, timed on this host's
 cores on a bounded token sample of the same workload (rank 0 only).
 
+--pass train: one step = moe_forward keeping its state + moe_backward (every
+gradient of <dy, y> + L_aux + z_coef * z_loss) with a seeded dy; the metric
+becomes training-step tokens/sec, and the roofline entry is the longest
+kernel of the step.
+
 With torchrun (N > 1) every rank runs its own replica of the layer on its
 own GPU (the layer has no cross-token exchange): weak scaling, no collective
 on the data path; only the timing is reduced across ranks.
@@ -256,6 +261,36 @@ def algorithmic_work(w, kept, offsets_active):
             "layer": (layer_flops, layer_bytes)}
 
 
+def backward_work(w, kept, active):
+    """FLOPs and bytes of the backward products (bf16 SwiGLU layers), per
+    launch, and of the whole training step (forward + backward).
+    down dgrad:    dh = dout W_down (2 A d F); reads the active down weights,
+                   dout, the kept pre-activations, writes their gradients.
+    down wgrad:    dW_down = dout^T h (2 A d F); reads dout, h; writes dW_down
+                   of every expert (fp32).
+    gate/up dgrad: dx_perm = da W_gate + db W_up (4 A d F); reads the active
+                   gate and up weights and (da | db); writes dx_perm (fp32).
+    gate/up wgrad: dW_gate, dW_up (4 A d F); reads (da | db), x_perm; writes
+                   both gradients of every expert (fp32).
+    step:          the forward's work, plus 2x its FLOPs; the weights read
+                   again, every weight gradient written, dy read, dx written."""
+    A, act = int(kept), int(active)
+    d, F = w.d, w.F
+    es = 2 if w.dtype == "bf16" else 4
+    E = w.N + w.n_shared
+    fwd = algorithmic_work(w, kept, active)
+    out = {
+        "bwd_down_dgrad": (2.0 * A * d * F, act * F * d * es + A * d * es + 2 * A * 2 * F * es),
+        "bwd_down_wgrad": (2.0 * A * d * F, A * d * es + A * F * es + E * d * F * 4),
+        "bwd_gate_up_dgrad": (4.0 * A * d * F, 2 * act * F * d * es + A * 2 * F * es + A * d * 4),
+        "bwd_gate_up_wgrad": (4.0 * A * d * F, A * 2 * F * es + A * d * es + E * 2 * F * d * 4),
+    }
+    fl, by = fwd["layer"]
+    out["step"] = (3.0 * fl, by + act * 3 * F * d * es + E * 3 * F * d * 4 +
+                   w.T * d * (es + 4) + 2 * w.N * d * 4)
+    return out
+
+
 def roofline_entry(flops, nbytes, seconds, peaks, sustained=False):
     """The bound (tensor or HBM) whose roofline time is larger, with the
     achieved rate and its fraction of the measured peak. sustained selects the
@@ -376,8 +411,11 @@ def workload_config(w, args, extra=None):
 def selected_workload(args):
     import dataclasses
     w = moe_inputs.WORKLOADS[args.workload]
-    return dataclasses.replace(w, gate_mode=args.gate_mode,
-                               select_bias="uniform" if args.select_bias else "none")
+    w = dataclasses.replace(w, gate_mode=args.gate_mode,
+                            select_bias="uniform" if args.select_bias else "none")
+    if args.tokens is not None:  # a smaller batch of the same layer (profiling captures)
+        w = dataclasses.replace(w, T=args.tokens)
+    return w
 
 
 def run_ours(args, world, rank):
@@ -507,6 +545,138 @@ def run_ours(args, world, rank):
     return 0
 
 
+def run_train(args, world, rank):
+    """Training step: moe_forward (keeping its state) + moe_backward."""
+    import mixture_experts_layer_101_b300 as moe
+
+    moe.load_library()
+    w = selected_workload(args)
+    if w.dtype != "bf16" or w.activation != "swiglu":
+        raise SystemExit("--pass train times bf16 SwiGLU layers")
+    cfg = moe.LayerConfig.from_workload(w)
+    cfg.save_for_backward = True
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sb = moe_inputs.make_select_bias(w)
+    cfg.select_bias = None if sb is None else sb.to(dev)
+    x = moe_inputs.make_x(w).to(dev)
+    dy = moe_inputs.make_dy(w).to(dev)
+    w_r, b_r = moe_inputs.make_router(w)
+    w_r = w_r.to(dev)
+    b_r = None if b_r is None else b_r.to(dev)
+    experts = moe_inputs.make_experts(w, dev)
+    layer = moe.MoELayer(cfg, w_r, b_r, experts, device=dev)
+    grads = moe.alloc_grads(cfg, b_r is not None, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    z = args.z_coef
+    nf, nb = len(moe.TRACE_STAGES) + 1, len(moe.TRACE_STAGES_BWD) + 1
+
+    for _ in range(args.warmup):
+        layer.forward(x)
+        layer.backward(dy, z, grads)
+    torch.cuda.synchronize()
+    layer.stats.status.zero_()
+    events = [moe.TraceEvents(nf + nb) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler() as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            h = events[i].handles()
+            moe.moe_trace_events(h[:nf])
+            layer.forward(x)
+            moe.moe_trace_events(h[nf:])
+            layer.backward(dy, z, grads)
+        moe.moe_trace_events([])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    step_ms = [ev.elapsed_ms(0, nf + nb - 1) for ev in events]
+    stage_ms = {name: [ev.elapsed_ms(j, j + 1) for ev in events]
+                for j, name in enumerate(moe.TRACE_STAGES)}
+    stage_ms.update({name: [ev.elapsed_ms(nf + j, nf + j + 1) for ev in events]
+                     for j, name in enumerate(moe.TRACE_STAGES_BWD)})
+    max_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    value = sum_over_ranks(float(w.T * args.steps), world) / max_s
+    st = layer.stats.to_host()
+    if st["status"] != 0:
+        raise SystemExit(f"device status word {st['status']:#x} after the timed steps")
+    if not all(bool(torch.isfinite(g).all()) for g in grads.values() if g is not None):
+        raise SystemExit("non-finite gradient after the timed steps")
+    kept = int(st["kept"].sum()) + w.n_shared * w.T
+    active = int((st["kept"] > 0).sum()) + w.n_shared
+    fw, bw = algorithmic_work(w, kept, active), backward_work(w, kept, active)
+    work = {"ffn_gate_up": fw["gate_up"], "ffn_down": fw["down"], **bw}
+    means = {k: statistics.mean(v) / 1e3 for k, v in stage_ms.items()}
+    dominant = max((k for k in work if k in means), key=lambda k: means[k])
+    ck = clocks.summary()
+    sustained = ("sw_power_cap" in ck["reasons"] and ck["sm_mhz"] is not None and
+                 ck["sm_max_mhz"] and ck["sm_mhz"] < 0.9 * ck["sm_max_mhz"])
+    peaks = measured_peaks()
+    roof = roofline_entry(*work[dominant], means[dominant], peaks, sustained)
+    roof["kernel"] = dominant
+    roof["traffic"] = None
+    roof["peak_source"] = (f"{peaks['source']} bf16 "
+                           + ("sustained (run power-capped)" if sustained else "burst")
+                           if roof["bound"] == "tensor" else f"{peaks['source']} HBM copy")
+    step_roof = roofline_entry(*bw["step"], statistics.mean(step_ms) / 1e3, peaks, sustained)
+
+    # end to end on host buffers: x and dy copied in from pinned memory, dx
+    # and L_aux copied out, every step
+    es = 2
+    x_h = moe_inputs.make_x(w).pin_memory()
+    dy_h = moe_inputs.make_dy(w).pin_memory()
+    dx_h = torch.empty((w.T, w.d), dtype=torch.float32).pin_memory()
+    laux_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    x_d, dy_d = torch.empty_like(x), torch.empty_like(dy)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        dy_d.copy_(dy_h, non_blocking=True)
+        layer.forward(x_d)
+        layer.backward(dy_d, z, grads)
+        dx_h.copy_(grads["dx"], non_blocking=True)
+        laux_h.copy_(layer.stats.l_aux, non_blocking=True)
+
+    for _ in range(min(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    barrier(world)
+    e2e_value = sum_over_ranks(float(w.T * args.steps), world) / max_over_ranks(e2e_s, world)
+
+    if rank == 0:
+        line = {
+            "metric": "MoE-layer training-step tokens/sec (forward + backward) and % of "
+                      "roofline, 1×B300",
+            "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * max_s / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": workload_config(w, args, {"pass": "train", "z_coef": z}),
+            "roofline": roof,
+            "step_roofline": dict(step_roof, note="whole training step against "
+                                                  "max(F/peak, B/BW) of its algorithmic work"),
+            "stage_ms": {k: round(statistics.mean(v), 4) for k, v in stage_ms.items()},
+            "kept_assignments": kept, "active_experts": active,
+            "cpu_baseline": None,
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
+                    "h2d_bytes_per_step": 2 * w.T * w.d * es,
+                    "d2h_bytes_per_step": w.T * w.d * 4 + 4},
+            "gpu_launches": (moe.forward_launch_count(cfg) + moe.backward_launch_count(cfg))
+            * args.steps,
+            "clocks": ck,
+            "wall_s_timed_region": round(wall, 4),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -519,6 +689,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gate-mode", default="renorm", choices=["renorm", "softmax"],
                     help="renorm: softmax over the K selected logits; softmax: full-softmax gate")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (small profiling cases)")
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "train"],
+                    help="forward (the layer's metric) or train: forward + backward")
+    ap.add_argument("--z-coef", type=float, default=1e-3,
+                    help="z-loss weight in the training objective (--pass train)")
     ap.add_argument("--select-bias", action="store_true",
                     help="add a seeded top-K selection bias (auxiliary-loss-free balancing)")
     args = ap.parse_args(argv)
@@ -528,6 +704,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
+        if args.pass_ == "train":
+            return run_train(args, world, rank)
         return run_ours(args, world, rank)
     finally:
         if world > 1:

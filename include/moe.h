@@ -330,14 +330,21 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* w_r,
                         void* ws, moe_stream_t stream);
 
 /* Tracing (instrumentation; the pages have no counterpart). Registers up to
- * 6 caller-created CUDA events (cudaEvent_t, passed as void*) for the
- * calling host thread; n = 0 clears them. While registered, moe_forward
- * records them on its stream at its stage boundaries:
- *   events[0] before the router, [1] after the router and statistics,
- *   [2] after the dispatch, [3] after the gate/up (or first Linear) grouped
- *   GEMM, [4] after the down grouped GEMM, [5] after the combine.
- * The library does not own, create or destroy the events.
- * Errors: MOE_ERR_INVALID (n outside [0, 6], or events NULL with n > 0). */
+ * 8 caller-created CUDA events (cudaEvent_t, passed as void*) for the
+ * calling host thread; n = 0 clears them. While registered, moe_forward and
+ * moe_backward record them on their stream at their stage boundaries:
+ *   moe_forward:  [0] before the router, [1] after the router and
+ *     statistics, [2] after the dispatch, [3] after the gate/up (or first
+ *     Linear) grouped GEMM, [4] after the down grouped GEMM, [5] after the
+ *     combine;
+ *   moe_backward: [0] at the start, [1] after the combine and router
+ *     backward, [2] after the down projection's input gradient, [3] after
+ *     its weight gradient, [4] after the first projection's input gradient,
+ *     [5] after its weight gradient, [6] after dx, [7] after the router
+ *     weight gradient.
+ * Events beyond n are not recorded. The library does not own, create or
+ * destroy the events.
+ * Errors: MOE_ERR_INVALID (n outside [0, 8], or events NULL with n > 0). */
 moe_status moe_trace_events(void* const* events, int32_t n);
 
 /* Self-test of failure detection (the pages have no counterpart). Launches

@@ -423,6 +423,7 @@ moe_status expert_bwd_simt(const moe_config& c, int64_t rows, const int32_t* off
         dout, d, wd, nullptr, d, static_cast<size_t>(d) * F, F, offsets, E, 0, F, d, nullptr, 0,
         pre, 2 * F);
   if (!ok()) return MOE_ERR_CUDA;
+  trace_record(2, s);
   // 4: dW_down[e] = dout_e^T h_e  ([d][F] per expert)
   gemm_wgrad_simt<Tx, Tx><<<dim3((d + BM - 1) / BM, (F + BN - 1) / BN, E), kThreads, 0, s>>>(
       dout, d, 0, h, F, 0, offsets, 0, E, 1, d, F, dwd);
@@ -432,11 +433,13 @@ moe_status expert_bwd_simt(const moe_config& c, int64_t rows, const int32_t* off
         dout, d, offsets, 0, E, 1, d, gr.db2);
     if (!ok()) return MOE_ERR_CUDA;
   }
+  trace_record(3, s);
   // 5: dx_perm = dpre_gate . W_gate + dpre_up . W_up (B_g(k = f, n = j) = W[e][f][j])
   gemm_rows_simt<Tx, Tx, EPI_STORE, Tx><<<gD, kThreads, 0, s>>>(
       pre, 2 * F, w1, wu, F, static_cast<size_t>(F) * d, d, offsets, E, 0, d,
       swiglu ? 2 * F : F, dxp, d, nullptr, 0);
   if (!ok()) return MOE_ERR_CUDA;
+  trace_record(4, s);
   // 6: dW_gate[e] = dpre_gate_e^T x_perm_e ([F][d]); dW_up from columns F..2F
   const dim3 gw((F + BM - 1) / BM, (d + BN - 1) / BN, E);
   gemm_wgrad_simt<Tx, Tx><<<gw, kThreads, 0, s>>>(pre, 2 * F, 0, x_perm, d, 0, offsets, 0, E, 1,
@@ -451,6 +454,7 @@ moe_status expert_bwd_simt(const moe_config& c, int64_t rows, const int32_t* off
         pre, 2 * F, offsets, 0, E, 1, F, gr.db1);
     if (!ok()) return MOE_ERR_CUDA;
   }
+  trace_record(5, s);
   return MOE_OK;
 }
 
@@ -494,6 +498,7 @@ moe_status backward_t(const moe_config& c, const WsLayout& L, void* ws, const Tx
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
+  trace_record(0, s);
   // 1
   combine_bwd_kernel<Tx><<<T, kThreads, 0, s>>>(dy, o, slot_of, gate, K, S, d, dout, dg);
   if (!ok()) return MOE_ERR_CUDA;
@@ -508,7 +513,8 @@ moe_status backward_t(const moe_config& c, const WsLayout& L, void* ws, const Tx
   else MOE_RBWD(8);
 #undef MOE_RBWD
   if (!ok()) return MOE_ERR_CUDA;
-  // 3-6
+  trace_record(1, s);
+  // 3-6 (trace events 2-5 after each of the four products)
   moe_status r = MOE_ERR_UNSUPPORTED;
   if (ffn_bwd_tc_supported(c))
     r = launch_ffn_bwd_tc(c, rows, offsets, w, x_perm, h, pre, dout, o, gr, status, s);
@@ -523,6 +529,7 @@ moe_status backward_t(const moe_config& c, const WsLayout& L, void* ws, const Tx
       <<<dim3(row_tiles(T, 1), (d + BN - 1) / BN), kThreads, 0, s>>>(
           dl, N, w_r, nullptr, N, 0, d, nullptr, 1, T, d, N, gr.dx, d, nullptr, 0);
   if (!ok()) return MOE_ERR_CUDA;
+  trace_record(6, s);
   // 9: dW_r = dl^T x, db_r = column sums of dl (split over tokens, then reduced)
   const int sp = L.rsplits;
   gemm_wgrad_simt<float, Tx><<<dim3((N + BM - 1) / BM, (d + BN - 1) / BN, sp), kThreads, 0, s>>>(
@@ -541,6 +548,7 @@ moe_status backward_t(const moe_config& c, const WsLayout& L, void* ws, const Tx
     reduce_splits_kernel<<<1, kThreads, 0, s>>>(bpart, sp, N, gr.db_r);
     if (!ok()) return MOE_ERR_CUDA;
   }
+  trace_record(7, s);
   return MOE_OK;
 }
 

@@ -57,7 +57,10 @@ struct BwShape {
   static constexpr int STAGES = (196608 / STAGE) > 6 ? 6 : (196608 / STAGE);
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + NUM_BARS * 8 + 16 + 2 * (MAX_GROUPS + 1) * 4;
+  // + per-epilogue-warp staging of a 32 x 32 fp32 block (row pitch 36 floats)
+  static constexpr int STG_FLOATS = 32 * 36;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + NUM_BARS * 8 + 16 +
+                              2 * (MAX_GROUPS + 1) * 4 + 16 + 4 * STG_FLOATS * 4;
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32_major(BM, BN, KIND == WGRAD, true);
 };
 
@@ -97,6 +100,8 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
   int* seg_off = tile_start + (MAX_GROUPS + 1);
+  float* staging = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(seg_off + MAX_GROUPS + 1) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.groups;
@@ -325,55 +330,85 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int r = m * BM + q * 32 + lane;  // row of the tile this thread drains
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
-      if (W) {
-        float* dst;
-        if (args.out2 != nullptr && r >= args.m_split)
-          dst = args.out2 + (static_cast<size_t>(e) * args.m_split + (r - args.m_split)) * args.ldo;
-        else
-          dst = args.out + (static_cast<size_t>(e) * (args.out2 ? args.m_split : args.m_blocks * BM) +
-                            r) * args.ldo;
-        dst += n * BN;
-        if (cnt == 0) {
-          for (int c = 0; c < BN; c += 4)
-            *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (W || KIND == DGRAD_STORE) {
+        // fp32 rows through a shared-memory transpose: the thread that owns
+        // TMEM lane `lane` writes its 32 values as one staging row, then
+        // each group of 8 lanes stores one 128-byte row segment (4 rows per
+        // instruction, whole sectors) instead of 32 scattered 16-byte pieces.
+        float* stg = staging + q * Sh::STG_FLOATS;
+        const int r0 = m * BM + q * 32;  // first tile row of this warp
+        float* rowbase;                   // row r0 of the output, at this tile's columns
+        int nvalid;                       // rows of the warp's 32 that are stored
+        if (W) {
+          const bool second = args.out2 != nullptr && m * BM >= args.m_split;
+          const int mrows = args.out2 ? args.m_split : args.m_blocks * BM;
+          rowbase = (second ? args.out2 + (static_cast<size_t>(e) * args.m_split +
+                                           (r0 - args.m_split)) * args.ldo
+                            : args.out + (static_cast<size_t>(e) * mrows + r0) * args.ldo) +
+                    n * BN;
+          nvalid = 32;
         } else {
+          rowbase = args.out + (static_cast<size_t>(seg_off[e]) + r0) * args.ldo + n * BN;
+          nvalid = min(32, max(0, cnt - r0));
+        }
+        const int sub = lane >> 3, col4 = (lane & 7) * 4;
+        if (W && cnt == 0) {
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+            for (int it = 0; it < 8; ++it)
+              *reinterpret_cast<float4*>(rowbase + static_cast<size_t>(it * 4 + sub) * args.ldo +
+                                         c * 32 + col4) = z;
+        } else if (nvalid > 0) {
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             uint32_t v[32];
             tmem_ld32(taddr + c * 32, v);
             tmem_ld_wait();
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+            float4* my = reinterpret_cast<float4*>(stg + lane * 36);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+              my[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int row = it * 4 + sub;
+              if (row < nvalid)
+                *reinterpret_cast<float4*>(rowbase + static_cast<size_t>(row) * args.ldo +
+                                           c * 32 + col4) =
+                    *reinterpret_cast<const float4*>(stg + row * 36 + col4);
+            }
+            __syncwarp();
           }
         }
       } else {
         const bool valid = r < cnt;
         const size_t grow = static_cast<size_t>(seg_off[e]) + static_cast<size_t>(r);
-        if (KIND == DGRAD_STORE) {
-          float* dst = args.out + grow * args.ldo + n * BN;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(taddr + c * 32, v);
-            tmem_ld_wait();
-            if (valid) {
-              float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                    __uint_as_float(v[4 * j + 2]),
-                                    __uint_as_float(v[4 * j + 3]));
-            }
-          }
-        } else {
-          // (a, b) -> (dh b silu'(a), dh silu(a)), bf16, in place
+        {
+          // (a, b) -> (dh b silu'(a), dh silu(a)), bf16, in place. The next
+          // chunk's (a, b) are loaded while this chunk's accumulator is read
+          // and processed, so the global latency overlaps the TMEM read.
           __nv_bfloat16* pa = args.pre + grow * 2 * args.F + n * BN;
           __nv_bfloat16* pb = pa + args.F;
+          uint4 ua[4], ub[4];
+          if (valid) {
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              ua[w4] = reinterpret_cast<const uint4*>(pa)[w4];
+              ub[w4] = reinterpret_cast<const uint4*>(pb)[w4];
+            }
+          }
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
+            uint4 na[4], nb[4];
+            if (valid && c + 1 < BN / 32) {
+#pragma unroll
+              for (int w4 = 0; w4 < 4; ++w4) {
+                na[w4] = reinterpret_cast<const uint4*>(pa + (c + 1) * 32)[w4];
+                nb[w4] = reinterpret_cast<const uint4*>(pb + (c + 1) * 32)[w4];
+              }
+            }
             uint32_t v[32];
             tmem_ld32(taddr + c * 32, v);
             tmem_ld_wait();
@@ -382,9 +417,8 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               uint4* qb = reinterpret_cast<uint4*>(pb + c * 32);
 #pragma unroll
               for (int w4 = 0; w4 < 4; ++w4) {
-                uint4 ua = qa[w4], ub = qb[w4];
-                uint32_t* ea = reinterpret_cast<uint32_t*>(&ua);
-                uint32_t* eb = reinterpret_cast<uint32_t*>(&ub);
+                uint32_t* ea = reinterpret_cast<uint32_t*>(&ua[w4]);
+                uint32_t* eb = reinterpret_cast<uint32_t*>(&ub[w4]);
 #pragma unroll
                 for (int p2 = 0; p2 < 4; ++p2) {
                   const float2 a2 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&ea[p2]));
@@ -400,9 +434,14 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                   ea[p2] = *reinterpret_cast<const uint32_t*>(&da);
                   eb[p2] = *reinterpret_cast<const uint32_t*>(&db);
                 }
-                qa[w4] = ua;
-                qb[w4] = ub;
+                qa[w4] = ua[w4];
+                qb[w4] = ub[w4];
               }
+            }
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              ua[w4] = na[w4];
+              ub[w4] = nb[w4];
             }
           }
         }
@@ -516,6 +555,7 @@ moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, const int32_t* o
     err = f256 ? launch<DGRAD_SWIGLU, 256>(m_dout128, m_wd, m_wd, a, mt_bound * a.n_tiles, s)
                : launch<DGRAD_SWIGLU, 128>(m_dout128, m_wd, m_wd, a, mt_bound * a.n_tiles, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace_record(2, s);
   }
   // 2. dW_down[e] = dout_e^T h_e: M = d, N = F
   {
@@ -525,6 +565,7 @@ moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, const int32_t* o
     err = f256 ? launch<WGRAD, 256>(m_dout64, m_h, m_h, a, tiles, s)
                : launch<WGRAD, 128>(m_dout64, m_h, m_h, a, tiles, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace_record(3, s);
   }
   // 3. dx_perm = da . W_gate + db . W_up: K = 2F (first F from W_gate), N = d
   {
@@ -532,6 +573,7 @@ moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, const int32_t* o
              F, status};
     err = launch<DGRAD_STORE, 256>(m_pre128, m_wg, m_wu, a, mt_bound * a.n_tiles, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace_record(4, s);
   }
   // 4. dW_gate | dW_up [e] = (da | db)_e^T x_perm_e: M = 2F rows split at F, N = d
   {
@@ -540,6 +582,7 @@ moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, const int32_t* o
     const int64_t tiles = static_cast<int64_t>(E) * a.m_blocks * a.n_tiles;
     err = launch<WGRAD, 256>(m_pre64, m_x, m_x, a, tiles, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
+    trace_record(5, s);
   }
   return MOE_OK;
 }

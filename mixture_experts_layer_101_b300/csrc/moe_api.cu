@@ -116,6 +116,17 @@ WsLayout ws_layout(const moe_config* c) {
   return L;
 }
 
+namespace {
+// Per-thread trace registration (moe_trace_events).
+constexpr int kMaxTrace = 8;
+thread_local cudaEvent_t g_trace[kMaxTrace] = {};
+thread_local int g_ntrace = 0;
+}  // namespace
+
+void trace_record(int i, cudaStream_t s) {
+  if (i < g_ntrace && g_trace[i] != nullptr) cudaEventRecord(g_trace[i], s);
+}
+
 int sm_count() {
   static int counts[64] = {0};
   static std::mutex mu;
@@ -164,14 +175,9 @@ moe_status check_weights(const moe_config* c, const moe_expert_weights* w) {
 }
 
 // Per-thread trace: events recorded on the launch stream at the stage
-// boundaries of moe_forward (see moe_trace_events).
-constexpr int kMaxTrace = 6;
-thread_local cudaEvent_t g_trace[kMaxTrace] = {};
-thread_local int g_ntrace = 0;
+// boundaries of moe_forward and moe_backward (see moe_trace_events).
 
-void trace(int i, cudaStream_t s) {
-  if (i < g_ntrace && g_trace[i] != nullptr) cudaEventRecord(g_trace[i], s);
-}
+void trace(int i, cudaStream_t s) { trace_record(i, s); }
 
 moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offsets,
                     const moe_expert_weights* w, float* o, moe_stats* stats, void* ws,

@@ -88,6 +88,9 @@ int64_t a_max_of(const moe_config* c);
 int64_t rows_max_of(const moe_config* c);  // routed A_max + n_shared * T
 WsLayout ws_layout(const moe_config* c);
 int sm_count();
+// Records the i-th event registered by moe_trace_events for this host thread
+// on stream s (nothing if fewer are registered).
+void trace_record(int i, cudaStream_t s);
 
 // ---- launchers (each returns MOE_OK or MOE_ERR_CUDA) -----------------------
 // Tensor-core router plan: NP = experts padded to 32/64/128/256, NPT = experts

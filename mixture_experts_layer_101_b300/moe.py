@@ -389,9 +389,10 @@ def moe_backward(cfg: LayerConfig, x, w_r, weights: dict, dy, z_coef: float, gra
 
 
 def moe_trace_events(events):
-    """Register up to 6 raw CUDA event handles (ints, e.g. TraceEvents.handles)
-    that moe_forward records at its stage boundaries on this host thread;
-    pass [] to clear. The caller keeps the events alive while registered."""
+    """Register up to 8 raw CUDA event handles (ints, e.g. TraceEvents.handles)
+    that moe_forward / moe_backward record at their stage boundaries on this
+    host thread; pass [] to clear. The caller keeps the events alive while
+    registered."""
     lib = load_library()
     arr = (ctypes.c_void_p * max(len(events), 1))(*[ctypes.c_void_p(int(e)) for e in events])
     _check(lib.moe_trace_events(arr if events else None, len(events)), "moe_trace_events")
@@ -443,6 +444,9 @@ def moe_selftest_bounded_wait(limit_us: int, status, stream=None):
 
 
 TRACE_STAGES = ["router", "dispatch", "ffn_gate_up", "ffn_down", "combine"]
+# intervals between moe_backward's eight trace events
+TRACE_STAGES_BWD = ["bwd_combine_router", "bwd_down_dgrad", "bwd_down_wgrad",
+                    "bwd_gate_up_dgrad", "bwd_gate_up_wgrad", "bwd_dx", "bwd_router_wgrad"]
 
 
 class MoELayer:

@@ -119,7 +119,7 @@ def test_backward_zero_tokens_gives_zero_gradients():
     cfg.save_for_backward = True
     layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
     layer.forward(inp["x"])  # a valid pointer; no row of it is read
-    grads = moe.moe.alloc_grads(cfg, router_bias=True)
+    grads = moe.alloc_grads(cfg, router_bias=True)
     for v in grads.values():
         if v is not None:
             v.fill_(float("nan"))
