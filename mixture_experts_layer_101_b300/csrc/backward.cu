@@ -178,18 +178,26 @@ router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ 
 }
 
 // ---- 7. dx[t] = [residual] dy[t] + sum of dx_perm over t's slots --------------
+// accumulate: dx already holds the router term dl W_r, which is added first.
 template <typename Tx>
 __global__ void __launch_bounds__(kThreads)
 dx_gather_kernel(const Tx* __restrict__ dy, const float* __restrict__ dxp,
                  const int32_t* __restrict__ slot_of, int KS, int d, int add_residual,
-                 float* __restrict__ dx) {
+                 int accumulate, float* __restrict__ dx) {
   __shared__ int32_t s_slot[16];
   const int t = blockIdx.x;
   if (threadIdx.x < KS) s_slot[threadIdx.x] = slot_of[static_cast<size_t>(t) * KS + threadIdx.x];
   __syncthreads();
   for (int c = threadIdx.x * 4; c < d; c += kThreads * 4) {
-    float4 acc = add_residual ? load4(dy + static_cast<size_t>(t) * d + c)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = accumulate ? *reinterpret_cast<const float4*>(dx + static_cast<size_t>(t) * d + c)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (add_residual) {
+      const float4 r = load4(dy + static_cast<size_t>(t) * d + c);
+      acc.x += r.x;
+      acc.y += r.y;
+      acc.z += r.z;
+      acc.w += r.w;
+    }
     for (int k = 0; k < KS; ++k) {
       const int s = s_slot[k];
       if (s < 0) continue;
@@ -521,27 +529,44 @@ moe_status backward_t(const moe_config& c, const WsLayout& L, void* ws, const Tx
   if (r == MOE_ERR_UNSUPPORTED)
     r = expert_bwd_simt<Tx>(c, rows, offsets, w, x_perm, h, pre, dout, o, gr, s);
   if (r != MOE_OK) return r;
-  // 7
-  dx_gather_kernel<Tx><<<T, kThreads, 0, s>>>(dy, o, slot_of, K + S, d, c.add_residual, gr.dx);
-  if (!ok()) return MOE_ERR_CUDA;
-  // 8: dx += dl . W_r  (B(k = e, n = j) = W_r[e][j])
-  gemm_rows_simt<float, float, EPI_ACCUM, float>
-      <<<dim3(row_tiles(T, 1), (d + BN - 1) / BN), kThreads, 0, s>>>(
-          dl, N, w_r, nullptr, N, 0, d, nullptr, 1, T, d, N, gr.dx, d, nullptr, 0);
-  if (!ok()) return MOE_ERR_CUDA;
-  trace_record(6, s);
-  // 9: dW_r = dl^T x, db_r = column sums of dl (split over tokens, then reduced)
   const int sp = L.rsplits;
-  gemm_wgrad_simt<float, Tx><<<dim3((N + BM - 1) / BM, (d + BN - 1) / BN, sp), kThreads, 0, s>>>(
-      dl, N, 0, x, d, 0, nullptr, T, 1, sp, N, d, rpart);
-  if (!ok()) return MOE_ERR_CUDA;
-  const size_t nd = static_cast<size_t>(N) * d;
-  const unsigned redb = static_cast<unsigned>(std::min<size_t>((nd + kThreads - 1) / kThreads,
-                                                               static_cast<size_t>(sm_count()) * 8));
-  reduce_splits_kernel<<<redb, kThreads, 0, s>>>(rpart, sp, nd, gr.dw_r);
-  if (!ok()) return MOE_ERR_CUDA;
-  if (gr.db_r) {
-    float* bpart = rpart + static_cast<size_t>(sp) * nd;
+  if (router_bwd_tc_supported(c)) {
+    // 8 then 7: dx = dl W_r on the tensor cores, then the gather adds the
+    // residual and the expert input gradients; 9: dW_r on the tensor cores
+    r = launch_router_bwd_tc(c, router_bwd_tc_plan(c), dl, w_r, x, gr.dx, gr.dw_r,
+                             reinterpret_cast<__nv_bfloat16*>(at(L.r_ar)),
+                             reinterpret_cast<__nv_bfloat16*>(at(L.r_br)),
+                             reinterpret_cast<int32_t*>(at(L.r_goff)),
+                             reinterpret_cast<float*>(at(L.r_part)), status, s);
+    if (r != MOE_OK) return r;
+    dx_gather_kernel<Tx><<<T, kThreads, 0, s>>>(dy, o, slot_of, K + S, d, c.add_residual, 1,
+                                                gr.dx);
+    if (!ok()) return MOE_ERR_CUDA;
+    trace_record(6, s);
+  } else {
+    // 7
+    dx_gather_kernel<Tx><<<T, kThreads, 0, s>>>(dy, o, slot_of, K + S, d, c.add_residual, 0,
+                                                gr.dx);
+    if (!ok()) return MOE_ERR_CUDA;
+    // 8: dx += dl . W_r  (B(k = e, n = j) = W_r[e][j])
+    gemm_rows_simt<float, float, EPI_ACCUM, float>
+        <<<dim3(row_tiles(T, 1), (d + BN - 1) / BN), kThreads, 0, s>>>(
+            dl, N, w_r, nullptr, N, 0, d, nullptr, 1, T, d, N, gr.dx, d, nullptr, 0);
+    if (!ok()) return MOE_ERR_CUDA;
+    trace_record(6, s);
+    // 9: dW_r = dl^T x (split over tokens, then reduced)
+    gemm_wgrad_simt<float, Tx>
+        <<<dim3((N + BM - 1) / BM, (d + BN - 1) / BN, sp), kThreads, 0, s>>>(
+            dl, N, 0, x, d, 0, nullptr, T, 1, sp, N, d, rpart);
+    if (!ok()) return MOE_ERR_CUDA;
+    const size_t nd = static_cast<size_t>(N) * d;
+    const unsigned redb = static_cast<unsigned>(std::min<size_t>(
+        (nd + kThreads - 1) / kThreads, static_cast<size_t>(sm_count()) * 8));
+    reduce_splits_kernel<<<redb, kThreads, 0, s>>>(rpart, sp, nd, gr.dw_r);
+    if (!ok()) return MOE_ERR_CUDA;
+  }
+  if (gr.db_r) {  // db_r = column sums of dl (split over tokens, then reduced)
+    float* bpart = rpart + static_cast<size_t>(sp) * N * d;
     colsum_kernel<float><<<dim3((N + kThreads - 1) / kThreads, sp), kThreads, 0, s>>>(
         dl, N, nullptr, T, 1, sp, N, bpart);
     if (!ok()) return MOE_ERR_CUDA;
@@ -560,9 +585,9 @@ int backward_launch_count(const moe_config& c) {
   int n = 2;  // combine_bwd, router_bwd
   if (ffn_bwd_tc_supported(c)) n += ffn_bwd_tc_launches(c);
   else n += swiglu ? 5 : (c.has_bias ? 6 : 4);
-  n += 2;      // dx gather, dx += dl W_r
-  n += 2;      // dW_r partials, reduction
-  n += 2;      // db_r partials, reduction
+  if (router_bwd_tc_supported(c)) n += 5;  // split, dl W_r, gather, dW_r partials, reduction
+  else n += 4;                              // gather, dl W_r, dW_r partials, reduction
+  n += 2;                                   // db_r partials, reduction
   return n;
 }
 

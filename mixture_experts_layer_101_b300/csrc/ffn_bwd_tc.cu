@@ -37,6 +37,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace moe {
@@ -585,6 +586,124 @@ moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, const int32_t* o
     trace_record(5, s);
   }
   return MOE_OK;
+}
+
+
+// ---- router gradients on the tensor cores ------------------------------------
+// dx += dl W_r and dW_r = dl^T x for bf16 layers. dl (fp32) and W_r (fp32)
+// are split into bf16 pairs, dl = dl_hi + dl_lo and W_r = W_hi + W_mid, each
+// exact to 2^-16 relative; the products keep the three terms above that
+// level, dl_hi W_hi + dl_lo W_hi + dl_hi W_mid, as one reduction over
+// K = 3 NP (NP = N rounded up to 64): A_r = [dl_hi | dl_lo | dl_hi],
+// B_r = [W_hi ; W_hi ; W_mid]. dW_r takes A_r's first 2 NP columns as
+// 2 NP output rows (hi then lo parts of dl) against x, over token groups of
+// T / G rows each, and a fixed-order reduction adds groups and parts.
+namespace {
+
+__global__ void __launch_bounds__(256)
+router_bwd_prep_kernel(const float* __restrict__ dl, const float* __restrict__ w_r, int T, int N,
+                       int NP, int d, int G, __nv_bfloat16* __restrict__ ar,
+                       __nv_bfloat16* __restrict__ br, int32_t* __restrict__ goff) {
+  const size_t na = static_cast<size_t>(T) * NP, nb = static_cast<size_t>(NP) * d;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < na + nb;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    if (i < na) {
+      const size_t t = i / NP;
+      const int e = static_cast<int>(i % NP);
+      const float v = e < N ? dl[t * N + e] : 0.f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      __nv_bfloat16* row = ar + t * 3 * NP;
+      row[e] = hi;
+      row[NP + e] = lo;
+      row[2 * NP + e] = hi;
+    } else {
+      const size_t k = i - na;
+      const int e = static_cast<int>(k / d), j = static_cast<int>(k % d);
+      const float w = e < N ? w_r[static_cast<size_t>(e) * d + j] : 0.f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+      const __nv_bfloat16 mid = __float2bfloat16_rn(w - __bfloat162float(hi));
+      br[static_cast<size_t>(e) * d + j] = hi;
+      br[(static_cast<size_t>(NP) + e) * d + j] = hi;
+      br[(static_cast<size_t>(2 * NP) + e) * d + j] = mid;
+    }
+  }
+  if (blockIdx.x == 0) {
+    for (int g = threadIdx.x; g <= G; g += blockDim.x)
+      goff[g] = static_cast<int32_t>(static_cast<int64_t>(T) * g / G);
+    if (threadIdx.x == 0) {  // one group of all T rows, for dx
+      goff[G + 1] = 0;
+      goff[G + 2] = T;
+    }
+  }
+}
+
+// dW_r[e][j] = sum_g (P[g][e][j] + P[g][NP + e][j]), groups ascending.
+__global__ void __launch_bounds__(256)
+router_wgrad_reduce_kernel(const float* __restrict__ part, int G, int N, int NP, int d,
+                           float* __restrict__ dw_r) {
+  const size_t n = static_cast<size_t>(N) * d;
+  const size_t gs = static_cast<size_t>(2 * NP) * d;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t lo = static_cast<size_t>(NP) * d;
+    float s = 0.f;
+    for (int g = 0; g < G; ++g) s += part[g * gs + i] + part[g * gs + lo + i];
+    dw_r[i] = s;
+  }
+}
+
+}  // namespace
+
+bool router_bwd_tc_supported(const moe_config& c) {
+  return c.dtype == MOE_BF16 && c.d_model % 256 == 0 && c.T > 0;
+}
+
+RouterBwdPlan router_bwd_tc_plan(const moe_config& c) {
+  RouterBwdPlan p{};
+  p.NP = (c.n_experts + 63) / 64 * 64;
+  const int tiles_per_group = (2 * p.NP / BM) * (c.d_model / 256);
+  int G = (2 * 148 + tiles_per_group - 1) / tiles_per_group;  // about two waves of CTAs
+  G = G < 1 ? 1 : (G > 64 ? 64 : G);
+  if (G > c.T) G = c.T > 0 ? c.T : 1;
+  p.G = G;
+  return p;
+}
+
+moe_status launch_router_bwd_tc(const moe_config& c, const RouterBwdPlan& p, const float* dl,
+                                const float* w_r, const void* x, float* dx, float* dw_r,
+                                __nv_bfloat16* ar, __nv_bfloat16* br, int32_t* goff,
+                                float* part, uint32_t* status, cudaStream_t s) {
+  const int T = c.T, N = c.n_experts, d = c.d_model, NP = p.NP, G = p.G;
+  const size_t work = static_cast<size_t>(T) * NP + static_cast<size_t>(NP) * d;
+  const unsigned pb = static_cast<unsigned>(
+      std::min<size_t>((work + 255) / 256, static_cast<size_t>(sm_count()) * 16));
+  router_bwd_prep_kernel<<<pb, 256, 0, s>>>(dl, w_r, T, N, NP, d, G, ar, br, goff);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  CUtensorMap m_ar128, m_ar64, m_br, m_x;
+  if (!make_map(&m_ar128, ar, T, 3 * NP, 128) || !make_map(&m_ar64, ar, T, 3 * NP, 64) ||
+      !make_map(&m_br, br, 3 * NP, d, 64) || !make_map(&m_x, x, T, d, 64))
+    return MOE_ERR_CUDA;
+  // dx = dl W_r: one group of T rows, K = 3 NP, N = d (written; the gather adds the rest)
+  {
+    BwArgs a{goff + G + 1, 1, 3 * NP / BK, 3 * NP / BK, 0, d / 256, 0, 0, 0, dx, nullptr, d,
+             nullptr, 0, status};
+    const int64_t tiles = (static_cast<int64_t>(T) + BM - 1) / BM * (d / 256);
+    if (launch<DGRAD_STORE, 256>(m_ar128, m_br, m_br, a, tiles, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  // partial dW_r per token group: M = 2 NP rows (dl_hi | dl_lo), N = d
+  {
+    BwArgs a{goff, G, 0, 0, 0, d / 256, 2 * NP / BM, 2 * NP, 0, part, nullptr, d, nullptr, 0,
+             status};
+    const int64_t tiles = static_cast<int64_t>(G) * a.m_blocks * a.n_tiles;
+    if (launch<WGRAD, 256>(m_ar64, m_x, m_x, a, tiles, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  const size_t nd = static_cast<size_t>(N) * d;
+  const unsigned rb = static_cast<unsigned>(
+      std::min<size_t>((nd + 255) / 256, static_cast<size_t>(sm_count()) * 8));
+  router_wgrad_reduce_kernel<<<rb, 256, 0, s>>>(part, G, N, NP, d, dw_r);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

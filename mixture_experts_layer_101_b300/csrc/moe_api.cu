@@ -112,6 +112,12 @@ WsLayout ws_layout(const moe_config* c) {
   L.dg = take(bw ? T * K * 4 : 0);
   L.dl = take(bw ? T * N * 4 : 0);
   L.rpart = take(bw ? static_cast<size_t>(L.rsplits) * N * (d + 1) * 4 : 0);
+  const bool rtc = bw && router_bwd_tc_supported(*c);
+  const RouterBwdPlan rb = rtc ? router_bwd_tc_plan(*c) : RouterBwdPlan{0, 0};
+  L.r_ar = take(rtc ? T * 3 * rb.NP * 2 : 0);
+  L.r_br = take(rtc ? static_cast<size_t>(3) * rb.NP * d * 2 : 0);
+  L.r_goff = take(rtc ? static_cast<size_t>(rb.G + 3) * 4 : 0);
+  L.r_part = take(rtc ? static_cast<size_t>(rb.G) * 2 * rb.NP * d * 4 : 0);
   L.total = total;
   return L;
 }

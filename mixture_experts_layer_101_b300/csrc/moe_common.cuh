@@ -76,6 +76,11 @@ struct WsLayout {
   size_t dg;                  // [T][K] fp32 gate gradients
   size_t dl;                  // [T][N] fp32 logit gradients
   size_t rpart;               // [rsplits][N][d + 1] fp32 router-gradient partials
+  // tensor-core router gradients (bf16 layers with d % 256 == 0):
+  size_t r_ar;                // [T][3 NP] bf16: dl_hi | dl_lo | dl_hi
+  size_t r_br;                // [3 NP][d] bf16: W_hi ; W_hi ; W_mid
+  size_t r_goff;              // [G + 3] int32 token-group offsets, then {0, T}
+  size_t r_part;              // [G][2 NP][d] fp32 partial dW_r
   size_t total;
   int64_t a_max;
   int nblk_r, nblk_d, rsplits;
@@ -147,6 +152,18 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
 
 // Backward pass (backward.cu): every gradient, from the state moe_forward
 // kept in the workspace.
+// Tensor-core router gradients (ffn_bwd_tc.cu): NP = N rounded up to 64, G
+// token groups for the weight gradient's reduction.
+struct RouterBwdPlan {
+  int NP, G;
+};
+bool router_bwd_tc_supported(const moe_config& c);
+RouterBwdPlan router_bwd_tc_plan(const moe_config& c);
+moe_status launch_router_bwd_tc(const moe_config& c, const RouterBwdPlan& p, const float* dl,
+                                const float* w_r, const void* x, float* dx, float* dw_r,
+                                __nv_bfloat16* ar, __nv_bfloat16* br, int32_t* goff,
+                                float* part, uint32_t* status, cudaStream_t s);
+
 moe_status launch_backward(const moe_config& c, const WsLayout& L, void* ws, const void* x,
                            const float* w_r, const moe_expert_weights& w, const void* dy,
                            float z_coef, const moe_grads& g, uint32_t* status, cudaStream_t s);
