@@ -71,11 +71,14 @@ class MoEGradsC(ctypes.Structure):
 _lib = None
 
 
-def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libmoe.so (built in-tree); raises if it is missing."""
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libmoe.so: the in-tree build, or the file named by the environment
+    variable MOE_LIBRARY (another build of the same sources, e.g. to compare
+    two builds in one process tree); raises if it is missing."""
     global _lib
     if _lib is not None:
         return _lib
+    path = path or os.environ.get("MOE_LIBRARY") or LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(f"libmoe.so not found at {path}: build it with "
                            "`python -m mixture_experts_layer_101_b300.build`")
