@@ -415,6 +415,8 @@ def selected_workload(args):
                             select_bias="uniform" if args.select_bias else "none")
     if args.tokens is not None:  # a smaller batch of the same layer (profiling captures)
         w = dataclasses.replace(w, T=args.tokens)
+    if args.experts is not None:  # fewer experts of the same shape (profiling captures)
+        w = dataclasses.replace(w, N=args.experts, K=min(w.K, args.experts))
     return w
 
 
@@ -691,6 +693,8 @@ def main(argv=None):
                     help="renorm: softmax over the K selected logits; softmax: full-softmax gate")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small profiling cases)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the workload's expert count (small profiling cases)")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "train"],
                     help="forward (the layer's metric) or train: forward + backward")
     ap.add_argument("--z-coef", type=float, default=1e-3,

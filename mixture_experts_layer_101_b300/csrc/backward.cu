@@ -390,6 +390,19 @@ colsum_kernel(const TA* __restrict__ A, int lda, const int32_t* __restrict__ off
   out[(static_cast<size_t>(sp) * groups + g) * ncols + c] = s;
 }
 
+// part[b][e] = sum of dl[t][e] over the 256 tokens of block b, ascending
+// (thread e per column; N <= 256).
+__global__ void __launch_bounds__(kThreads)
+logit_colsum_kernel(const float* __restrict__ dl, int T, int N, float* __restrict__ part) {
+  const int e = threadIdx.x;
+  if (e >= N) return;
+  const int t0 = blockIdx.x * 256, t1 = min(T, t0 + 256);
+  float s = 0.f;
+#pragma unroll 8
+  for (int t = t0; t < t1; ++t) s += dl[static_cast<size_t>(t) * N + e];
+  part[static_cast<size_t>(blockIdx.x) * N + e] = s;
+}
+
 // out[i] = sum_{sp ascending} part[sp * n + i]
 __global__ void __launch_bounds__(kThreads)
 reduce_splits_kernel(const float* __restrict__ part, int splits, size_t n,
@@ -565,12 +578,12 @@ moe_status backward_t(const moe_config& c, const WsLayout& L, void* ws, const Tx
     reduce_splits_kernel<<<redb, kThreads, 0, s>>>(rpart, sp, nd, gr.dw_r);
     if (!ok()) return MOE_ERR_CUDA;
   }
-  if (gr.db_r) {  // db_r = column sums of dl (split over tokens, then reduced)
-    float* bpart = rpart + static_cast<size_t>(sp) * N * d;
-    colsum_kernel<float><<<dim3((N + kThreads - 1) / kThreads, sp), kThreads, 0, s>>>(
-        dl, N, nullptr, T, 1, sp, N, bpart);
+  if (gr.db_r) {  // db_r = column sums of dl: 256-token blocks, then a fixed-order reduction
+    float* bpart = reinterpret_cast<float*>(at(L.bpart));
+    const int nb = (T + 255) / 256;
+    logit_colsum_kernel<<<nb, kThreads, 0, s>>>(dl, T, N, bpart);
     if (!ok()) return MOE_ERR_CUDA;
-    reduce_splits_kernel<<<1, kThreads, 0, s>>>(bpart, sp, N, gr.db_r);
+    reduce_splits_kernel<<<1, kThreads, 0, s>>>(bpart, nb, N, gr.db_r);
     if (!ok()) return MOE_ERR_CUDA;
   }
   trace_record(7, s);

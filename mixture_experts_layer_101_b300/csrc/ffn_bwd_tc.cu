@@ -43,25 +43,34 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BK = 64, kThreads = 192;
+constexpr int BM = 128, BK = 64;
 constexpr int MAX_GROUPS = 264;
 constexpr int CHUNK = 64 * 128;  // one 64-column x 64-row MN-major box: 8 KB
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 enum { DGRAD_STORE = 0, DGRAD_SWIGLU = 1, WGRAD = 2 };
 
+// Epilogue warps: NEPI = 4 (one per TMEM lane quarter; 8, two per quarter
+// splitting the columns, measured slower for every kind). The staging buffers
+// for the fp32 transposes are 32 x 32 floats per epilogue warp, 16-byte
+// chunks XOR-swizzled by row (no padding, no bank conflicts).
 template <int KIND, int BN>
 struct BwShape {
+  static constexpr int NEPI = 4;
+  static constexpr int THREADS = 64 + 32 * NEPI;
+  static constexpr bool STAGED = KIND != DGRAD_SWIGLU;
   static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * BK * 2;  // 16 or 32 KB
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196608 / STAGE) > 6 ? 6 : (196608 / STAGE);
+  static constexpr int RING = (KIND == WGRAD && NEPI == 8) ? 147456 : 196608;
+  static constexpr int STAGES = (RING / STAGE) > 6 ? 6 : (RING / STAGE);
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
-  // + per-epilogue-warp staging of a 32 x 32 fp32 block (row pitch 36 floats)
-  static constexpr int STG_FLOATS = 32 * 36;
+  static constexpr int STG_FLOATS = 32 * 32;
   static constexpr int SMEM = 1024 + STAGES * STAGE + NUM_BARS * 8 + 16 +
-                              2 * (MAX_GROUPS + 1) * 4 + 16 + 4 * STG_FLOATS * 4;
+                              2 * (MAX_GROUPS + 1) * 4 + 16 +
+                              (STAGED ? NEPI * STG_FLOATS * 4 : 0);
+  static_assert(SMEM <= 232448, "shared memory");
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32_major(BM, BN, KIND == WGRAD, true);
 };
 
@@ -84,7 +93,7 @@ struct BwArgs {
 };
 
 template <int KIND, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BwShape<KIND, BN>::THREADS, 1)
 grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const BwArgs args) {
   using namespace ptx;
@@ -102,7 +111,8 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
   int* seg_off = tile_start + (MAX_GROUPS + 1);
   float* staging = reinterpret_cast<float*>(
-      (reinterpret_cast<uintptr_t>(seg_off + MAX_GROUPS + 1) + 15) & ~static_cast<uintptr_t>(15));
+      (reinterpret_cast<uintptr_t>(seg_off + MAX_GROUPS + 1) + 15) &
+      ~static_cast<uintptr_t>(15));  // STAGED kinds only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.groups;
@@ -119,7 +129,7 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
-      mbar_init(bar_tempty(a), 4);
+      mbar_init(bar_tempty(a), Sh::NEPI);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -314,7 +324,12 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue ----
-    const int q = warp & 3;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // column chunks of this warp: all, or one half when two warps share q
+    constexpr int NCH = BN / 32;
+    const int half = (warp - 2) >> 2;
+    const int c_begin = Sh::NEPI == 8 ? half * (NCH / 2) : 0;
+    const int c_end = Sh::NEPI == 8 ? c_begin + NCH / 2 : NCH;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -336,7 +351,7 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // TMEM lane `lane` writes its 32 values as one staging row, then
         // each group of 8 lanes stores one 128-byte row segment (4 rows per
         // instruction, whole sectors) instead of 32 scattered 16-byte pieces.
-        float* stg = staging + q * Sh::STG_FLOATS;
+        float* stg = staging + (warp - 2) * Sh::STG_FLOATS;
         const int r0 = m * BM + q * 32;  // first tile row of this warp
         float* rowbase;                   // row r0 of the output, at this tile's columns
         int nvalid;                       // rows of the warp's 32 that are stored
@@ -352,25 +367,27 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           rowbase = args.out + (static_cast<size_t>(seg_off[e]) + r0) * args.ldo + n * BN;
           nvalid = min(32, max(0, cnt - r0));
         }
-        const int sub = lane >> 3, col4 = (lane & 7) * 4;
+        const int sub = lane >> 3, q4 = lane & 7, col4 = q4 * 4;
         if (W && cnt == 0) {
           const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int c = 0; c < BN / 32; ++c)
+          for (int c = c_begin; c < c_end; ++c)
 #pragma unroll
             for (int it = 0; it < 8; ++it)
               *reinterpret_cast<float4*>(rowbase + static_cast<size_t>(it * 4 + sub) * args.ldo +
                                          c * 32 + col4) = z;
         } else if (nvalid > 0) {
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = c_begin; c < c_end; ++c) {
             uint32_t v[32];
             tmem_ld32(taddr + c * 32, v);
             tmem_ld_wait();
-            float4* my = reinterpret_cast<float4*>(stg + lane * 36);
+            // row `lane`, 16-byte chunk j stored at chunk j ^ (lane & 7)
+            float4* my = reinterpret_cast<float4*>(stg + lane * 32);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              my[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+              my[j ^ (lane & 7)] =
+                  make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                              __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
             __syncwarp();
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
@@ -378,7 +395,7 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               if (row < nvalid)
                 *reinterpret_cast<float4*>(rowbase + static_cast<size_t>(row) * args.ldo +
                                            c * 32 + col4) =
-                    *reinterpret_cast<const float4*>(stg + row * 36 + col4);
+                    *reinterpret_cast<const float4*>(stg + row * 32 + 4 * (q4 ^ (row & 7)));
             }
             __syncwarp();
           }
@@ -396,14 +413,14 @@ grouped_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (valid) {
 #pragma unroll
             for (int w4 = 0; w4 < 4; ++w4) {
-              ua[w4] = reinterpret_cast<const uint4*>(pa)[w4];
-              ub[w4] = reinterpret_cast<const uint4*>(pb)[w4];
+              ua[w4] = reinterpret_cast<const uint4*>(pa + c_begin * 32)[w4];
+              ub[w4] = reinterpret_cast<const uint4*>(pb + c_begin * 32)[w4];
             }
           }
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = c_begin; c < c_end; ++c) {
             uint4 na[4], nb[4];
-            if (valid && c + 1 < BN / 32) {
+            if (valid && c + 1 < c_end) {
 #pragma unroll
               for (int w4 = 0; w4 < 4; ++w4) {
                 na[w4] = reinterpret_cast<const uint4*>(pa + (c + 1) * 32)[w4];
@@ -516,7 +533,8 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
   const int64_t sms = sm_count();
   const unsigned grid = static_cast<unsigned>(tiles_bound < sms ? tiles_bound : sms);
   if (grid == 0) return cudaSuccess;
-  grouped_bwd_tc<KIND, BN><<<grid, kThreads, BwShape<KIND, BN>::SMEM, s>>>(a, b0, b1, args);
+  grouped_bwd_tc<KIND, BN><<<grid, BwShape<KIND, BN>::THREADS, BwShape<KIND, BN>::SMEM, s>>>(
+      a, b0, b1, args);
   return cudaGetLastError();
 }
 

@@ -112,6 +112,7 @@ WsLayout ws_layout(const moe_config* c) {
   L.dg = take(bw ? T * K * 4 : 0);
   L.dl = take(bw ? T * N * 4 : 0);
   L.rpart = take(bw ? static_cast<size_t>(L.rsplits) * N * (d + 1) * 4 : 0);
+  L.bpart = take(bw ? ((T + 255) / 256 > 0 ? (T + 255) / 256 : 1) * N * 4 : 0);
   const bool rtc = bw && router_bwd_tc_supported(*c);
   const RouterBwdPlan rb = rtc ? router_bwd_tc_plan(*c) : RouterBwdPlan{0, 0};
   L.r_ar = take(rtc ? T * 3 * rb.NP * 2 : 0);

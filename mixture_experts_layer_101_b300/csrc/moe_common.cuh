@@ -76,6 +76,7 @@ struct WsLayout {
   size_t dg;                  // [T][K] fp32 gate gradients
   size_t dl;                  // [T][N] fp32 logit gradients
   size_t rpart;               // [rsplits][N][d + 1] fp32 router-gradient partials
+  size_t bpart;               // [ceil(T/256)][N] fp32 partial column sums of dl (db_r)
   // tensor-core router gradients (bf16 layers with d % 256 == 0):
   size_t r_ar;                // [T][3 NP] bf16: dl_hi | dl_lo | dl_hi
   size_t r_br;                // [3 NP][d] bf16: W_hi ; W_hi ; W_mid
