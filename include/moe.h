@@ -361,8 +361,9 @@ moe_status moe_selftest_bounded_wait(uint32_t limit_us, uint32_t* status,
 const char* moe_status_string(moe_status s);
 
 /* Number of kernels one moe_forward call on cfg launches (with every member
- * of stats non-NULL), for accounting by benchmarks and tracers; -1 if cfg
- * is invalid. Instrumentation; the pages have no counterpart. */
+ * of stats non-NULL; one more with save_for_backward on the tensor-core
+ * path), for accounting by benchmarks and tracers; -1 if cfg is invalid.
+ * Instrumentation; the pages have no counterpart. */
 int32_t moe_forward_launch_count(const moe_config* cfg);
 
 /* Number of kernels one moe_backward call on cfg launches (with db_r

@@ -32,10 +32,13 @@
 
 namespace moe {
 
-// Tensor-core expert gradients (ffn_bwd_tc.cu); MOE_OK when done, else the
-// caller falls back to the CUDA-core kernels below.
+// Tensor-core expert gradients (ffn_bwd_tc.cu). dout and the pre-activations
+// (then their gradients, in place) live in the padded row space poff (each
+// expert's rows rounded up to 64, pad rows zero).
 bool ffn_bwd_tc_supported(const moe_config& c);
-moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, const int32_t* offsets,
+int64_t ffn_bwd_pad_rows(const moe_config& c);
+moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, int64_t rows_pad,
+                             const int32_t* offsets, const int32_t* poff,
                              const moe_expert_weights& w, const void* x_perm, const void* h,
                              void* pre, const void* dout, float* dx_perm, const moe_grads& g,
                              uint32_t* status, cudaStream_t s);
@@ -45,20 +48,103 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// ---- padded row space --------------------------------------------------------
+// poff[e] = sum over e' < e of (offsets[e'+1] - offsets[e']) rounded up to 64
+// (one warp; G <= 288).
+__global__ void pad_offsets_kernel(const int32_t* __restrict__ offsets, int G,
+                                   int32_t* __restrict__ poff) {
+  const int lane = threadIdx.x;
+  constexpr int PER = 9;
+  int loc[PER], sum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane * PER + j;
+    loc[j] = e < G ? (offsets[e + 1] - offsets[e] + 63) / 64 * 64 : 0;
+    sum += loc[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane * PER + j;
+    if (e < G) poff[e] = run;
+    run += loc[j];
+  }
+  if (lane == 31) poff[G] = incl;
+}
+
+}  // namespace
+
+moe_status launch_pad_offsets(const int32_t* offsets, int G, int32_t* poff, cudaStream_t s) {
+  pad_offsets_kernel<<<1, 32, 0, s>>>(offsets, G, poff);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+namespace {
+
+// Zero the pad rows [poff[e] + count, poff[e+1]) of a [rows][ld] bf16 buffer;
+// block e, at most 63 rows.
+__global__ void __launch_bounds__(kThreads)
+zero_pad_rows_kernel(__nv_bfloat16* __restrict__ buf, int ld, const int32_t* __restrict__ offsets,
+                     const int32_t* __restrict__ poff) {
+  const int e = blockIdx.x;
+  const int r0 = poff[e] + (offsets[e + 1] - offsets[e]), r1 = poff[e + 1];
+  const int per_row = ld / 8;  // 16-byte pieces
+  for (int i = threadIdx.x; i < (r1 - r0) * per_row; i += kThreads) {
+    const int r = r0 + i / per_row, c = i % per_row;
+    reinterpret_cast<uint4*>(buf + static_cast<size_t>(r) * ld)[c] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// The weight-gradient products reduce over whole 64-row steps of the padded
+// rows, so the last expert's step reads up to 63 forward rows past its end
+// (multiplied by zero rows of A). Those rows [offsets[G], offsets[G] + 63) of
+// x_perm and h are unused workspace: zero them (within rows_max) so that no
+// stale bit pattern (NaN, infinity) meets the zeros.
+__global__ void __launch_bounds__(kThreads)
+zero_tail_rows_kernel(__nv_bfloat16* __restrict__ x_perm, int d, __nv_bfloat16* __restrict__ h,
+                      int F, const int32_t* __restrict__ end, int64_t rows_max) {
+  const int64_t r0 = *end;
+  const int64_t r1 = min(rows_max, r0 + 63);
+  const int pd = d / 8, pf = F / 8;  // 16-byte pieces per row
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
+       i < (r1 - r0) * (pd + pf); i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t r = r0 + i / (pd + pf);
+    const int c = static_cast<int>(i % (pd + pf));
+    if (c < pd)
+      reinterpret_cast<uint4*>(x_perm + r * d)[c] = make_uint4(0u, 0u, 0u, 0u);
+    else
+      reinterpret_cast<uint4*>(h + r * F)[c - pd] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // ---- 1. combine backward -----------------------------------------------------
+// dout rows: slot s of expert e goes to row s - offsets[e] + poff[e] (poff ==
+// offsets: the dispatch's own rows).
 template <typename Tx>
 __global__ void __launch_bounds__(kThreads)
 combine_bwd_kernel(const Tx* __restrict__ dy, const float* __restrict__ o,
-                   const int32_t* __restrict__ slot_of, const float* __restrict__ gate, int K,
-                   int S, int d, Tx* __restrict__ dout, float* __restrict__ dg) {
-  __shared__ int32_t s_slot[16];
+                   const int32_t* __restrict__ slot_of, const float* __restrict__ gate,
+                   const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
+                   const int32_t* __restrict__ poff, int N, int K, int S, int d,
+                   Tx* __restrict__ dout, float* __restrict__ dg) {
+  __shared__ int32_t s_slot[16], s_prow[16];
   __shared__ float s_gate[16];
   __shared__ float s_red[kThreads / 32][8];
   const int t = blockIdx.x, KS = K + S;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x < KS) {
-    s_slot[threadIdx.x] = slot_of[static_cast<size_t>(t) * KS + threadIdx.x];
-    s_gate[threadIdx.x] = threadIdx.x < K ? gate[static_cast<size_t>(t) * K + threadIdx.x] : 1.f;
+    const int k = threadIdx.x;
+    const int slot = slot_of[static_cast<size_t>(t) * KS + k];
+    const int e = k < K ? idx[static_cast<size_t>(t) * K + k] : N + (k - K);
+    s_slot[k] = slot;
+    s_prow[k] = slot >= 0 ? slot - offsets[e] + poff[e] : -1;
+    s_gate[k] = k < K ? gate[static_cast<size_t>(t) * K + k] : 1.f;
   }
   __syncthreads();
   float part[8];
@@ -79,11 +165,11 @@ combine_bwd_kernel(const Tx* __restrict__ dy, const float* __restrict__ o,
       p = fmaf(g4.w, ov.w, p);
       part[k] = p;
       const float g = s_gate[k];
-      store4(dout + static_cast<size_t>(s) * d + c,
+      store4(dout + static_cast<size_t>(s_prow[k]) * d + c,
              make_float4(g * g4.x, g * g4.y, g * g4.z, g * g4.w));
     }
     for (int k = K; k < KS; ++k)  // shared experts: gate 1
-      store4(dout + static_cast<size_t>(s_slot[k]) * d + c, g4);
+      store4(dout + static_cast<size_t>(s_prow[k]) * d + c, g4);
   }
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -520,8 +606,22 @@ moe_status backward_t(const moe_config& c, const WsLayout& L, void* ws, const Tx
     return MOE_OK;
   }
   trace_record(0, s);
+  const bool tc = ffn_bwd_tc_supported(c);
+  // the tensor-core path keeps dout and the pre-activation gradients in the
+  // padded row space; the CUDA-core path in the dispatch's rows
+  int32_t* poff = reinterpret_cast<int32_t*>(at(L.poff));
+  if (tc) {  // poff: written by the forward (with the pre-activations)
+    zero_pad_rows_kernel<<<E, kThreads, 0, s>>>(reinterpret_cast<__nv_bfloat16*>(dout), d,
+                                                offsets, poff);
+    if (!ok()) return MOE_ERR_CUDA;
+    zero_tail_rows_kernel<<<16, kThreads, 0, s>>>(
+        reinterpret_cast<__nv_bfloat16*>(const_cast<Tx*>(x_perm)), d,
+        reinterpret_cast<__nv_bfloat16*>(const_cast<Tx*>(h)), F, offsets + E, rows);
+    if (!ok()) return MOE_ERR_CUDA;
+  }
   // 1
-  combine_bwd_kernel<Tx><<<T, kThreads, 0, s>>>(dy, o, slot_of, gate, K, S, d, dout, dg);
+  combine_bwd_kernel<Tx><<<T, kThreads, 0, s>>>(dy, o, slot_of, gate, idx, offsets,
+                                                tc ? poff : offsets, N, K, S, d, dout, dg);
   if (!ok()) return MOE_ERR_CUDA;
   // 2
   const unsigned rb = static_cast<unsigned>((T + kThreads / 32 - 1) / (kThreads / 32));
@@ -536,11 +636,9 @@ moe_status backward_t(const moe_config& c, const WsLayout& L, void* ws, const Tx
   if (!ok()) return MOE_ERR_CUDA;
   trace_record(1, s);
   // 3-6 (trace events 2-5 after each of the four products)
-  moe_status r = MOE_ERR_UNSUPPORTED;
-  if (ffn_bwd_tc_supported(c))
-    r = launch_ffn_bwd_tc(c, rows, offsets, w, x_perm, h, pre, dout, o, gr, status, s);
-  if (r == MOE_ERR_UNSUPPORTED)
-    r = expert_bwd_simt<Tx>(c, rows, offsets, w, x_perm, h, pre, dout, o, gr, s);
+  moe_status r = tc ? launch_ffn_bwd_tc(c, rows, ffn_bwd_pad_rows(c), offsets, poff, w, x_perm,
+                                        h, pre, dout, o, gr, status, s)
+                    : expert_bwd_simt<Tx>(c, rows, offsets, w, x_perm, h, pre, dout, o, gr, s);
   if (r != MOE_OK) return r;
   const int sp = L.rsplits;
   if (router_bwd_tc_supported(c)) {
@@ -596,7 +694,8 @@ int backward_launch_count(const moe_config& c) {
   if (c.T == 0) return 0;
   const bool swiglu = c.activation == MOE_SWIGLU;
   int n = 2;  // combine_bwd, router_bwd
-  if (ffn_bwd_tc_supported(c)) n += ffn_bwd_tc_launches(c);
+  // + pad rows of dout, tail rows of x_perm and h
+  if (ffn_bwd_tc_supported(c)) n += 2 + ffn_bwd_tc_launches(c);
   else n += swiglu ? 5 : (c.has_bias ? 6 : 4);
   if (router_bwd_tc_supported(c)) n += 5;  // split, dl W_r, gather, dW_r partials, reduction
   else n += 4;                              // gather, dl W_r, dW_r partials, reduction

@@ -77,8 +77,10 @@ struct TcArgs {
   void* out;               // h (bf16, row length F) or o (fp32, row length d)
   int ldo;
   uint32_t* status;
-  void* pre;               // gate/up: NULL, or [rows][2F] bf16 pre-activations
-                           // (gate | up) kept for the backward pass
+  void* pre;               // gate/up: NULL, or [padded rows][2F] bf16 pre-activations
+                           // (gate | up) kept for the backward pass, row poff[e] + r for
+                           // row r of expert e
+  const int32_t* poff;     // [N+1] padded row offsets (with pre)
 };
 
 // The 32 gate and 32 up pre-activations of one row chunk, rounded to bf16, at
@@ -341,7 +343,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
                                   packed[4 * v + 3]);
             if (args.pre != nullptr)
-              store_pre(static_cast<__nv_bfloat16*>(args.pre) + grow * 2 * args.ldo +
+              store_pre(static_cast<__nv_bfloat16*>(args.pre) +
+                            (static_cast<size_t>(args.poff[e]) + r) * 2 * args.ldo +
                             n * Sh::OUT_COLS + c * 32,
                         args.ldo, g, u);
           }
@@ -637,7 +640,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
               dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
                                   packed[4 * v + 3]);
             if (args.pre != nullptr)
-              store_pre(static_cast<__nv_bfloat16*>(args.pre) + grow * 2 * args.ldo + n * 128 +
+              store_pre(static_cast<__nv_bfloat16*>(args.pre) +
+                            (static_cast<size_t>(args.poff[e]) + r) * 2 * args.ldo + n * 128 +
                             c * 32,
                         args.ldo, g, u);
           }
@@ -772,7 +776,8 @@ bool ffn_tc_supported(const moe_config& c) {
 
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w, void* h, float* o,
-                         void* pre, uint32_t* status, cudaStream_t s, int part) {
+                         void* pre, const int32_t* poff, uint32_t* status, cudaStream_t s,
+                         int part) {
   if (rows == 0) return MOE_OK;
   const int E = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
   const bool pairs1 = use_pairs(c, rows, d);  // gate/up: reduction over d
@@ -787,7 +792,7 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
         !make_map(&mg, w.w_gate, static_cast<uint64_t>(E) * F, d, 128) ||
         !make_map(&mu, w.w_up, static_cast<uint64_t>(E) * F, d, 128))
       return MOE_ERR_CUDA;
-    TcArgs a1{offsets, E, d, F / 128, F, h, F, status, pre};
+    TcArgs a1{offsets, E, d, F / 128, F, h, F, status, pre, poff};
     if (pairs1) {
       if (launch_pair<0>(mx, mg, mu, a1, ptiles * (F / 128), s) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -807,7 +812,7 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
     if (!make_map(&mh, h, rows, F, 128) ||
         !make_map(&md, w.w_down, static_cast<uint64_t>(E) * d, F, pairs2 ? 128 : 256))
       return MOE_ERR_CUDA;
-    TcArgs a2{offsets, E, F, d / 256, d, o, d, status, nullptr};
+    TcArgs a2{offsets, E, F, d / 256, d, o, d, status, nullptr, nullptr};
     if (pairs2) {
       if (launch_pair<1>(mh, md, md, a2, ptiles * (d / 256), s) != cudaSuccess)
         return MOE_ERR_CUDA;

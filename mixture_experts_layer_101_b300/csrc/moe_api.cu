@@ -106,18 +106,21 @@ WsLayout ws_layout(const moe_config* c) {
   // router-gradient K splits: about 1024 tokens each, at most 32
   L.rsplits = bw ? static_cast<int>(std::min<size_t>(32, std::max<size_t>(1, T / 1024))) : 0;
   L.logits = take(bw ? T * N * 4 : 0);
-  L.pre = take(bw ? A * 2 * F * es : 0);
+  const bool ftc = bw && ffn_bwd_tc_supported(*c);
+  const size_t Apad = ftc ? static_cast<size_t>(ffn_bwd_pad_rows(*c)) : A;
+  L.pre = take(bw ? Apad * 2 * F * es : 0);
   L.count = take(bw ? N * 4 : 0);
-  L.dout = take(bw ? A * d * es : 0);
+  L.dout = take(bw ? Apad * d * es : 0);
+  L.poff = take(bw ? (N + S + 1) * 4 : 0);
   L.dg = take(bw ? T * K * 4 : 0);
   L.dl = take(bw ? T * N * 4 : 0);
   L.rpart = take(bw ? static_cast<size_t>(L.rsplits) * N * (d + 1) * 4 : 0);
   L.bpart = take(bw ? ((T + 255) / 256 > 0 ? (T + 255) / 256 : 1) * N * 4 : 0);
   const bool rtc = bw && router_bwd_tc_supported(*c);
   const RouterBwdPlan rb = rtc ? router_bwd_tc_plan(*c) : RouterBwdPlan{0, 0};
-  L.r_ar = take(rtc ? T * 3 * rb.NP * 2 : 0);
+  L.r_ar = take(rtc ? (T + 63) / 64 * 64 * 3 * rb.NP * 2 : 0);
   L.r_br = take(rtc ? static_cast<size_t>(3) * rb.NP * d * 2 : 0);
-  L.r_goff = take(rtc ? static_cast<size_t>(rb.G + 3) * 4 : 0);
+  L.r_goff = take(rtc ? static_cast<size_t>(2 * rb.G + 6) * 4 : 0);
   L.r_part = take(rtc ? static_cast<size_t>(rb.G) * 2 * rb.NP * d * 4 : 0);
   L.total = total;
   return L;
@@ -192,12 +195,17 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
   const WsLayout L = ws_layout(c);
   void* h = at(ws, L.h);
   void* pre = keep_pre ? at(ws, L.pre) : nullptr;
+  int32_t* poff = reinterpret_cast<int32_t*>(at(ws, L.poff));
+  if (keep_pre && ffn_tc_supported(*c)) {  // the tensor-core path keeps them in padded rows
+    const moe_status r = launch_pad_offsets(offsets, c->n_experts + c->n_shared, poff, s);
+    if (r != MOE_OK) return r;
+  }
   const bool tc = ffn_tc_supported(*c);
   uint32_t* status = stats ? stats->status : nullptr;
   for (int part = 1; part <= 2; ++part) {
     const int64_t rows = rows_max_of(c);
     const moe_status r =
-        tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, pre, status, s, part)
+        tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, pre, poff, status, s, part)
            : launch_ffn_simt(*c, rows, x_perm, offsets, *w, h, o, pre, s, part);
     if (r != MOE_OK) return r;
     if (traced) trace(2 + part, s);
@@ -232,7 +240,9 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   const int dispatch = 4;                               // histogram, scan, permute, gather
   const int ffn = 2;                                    // gate/up, down
   const int combine = 1;
-  return router + stats + dispatch + ffn + combine;
+  // keeping the pre-activations for the tensor-core backward: their padded offsets
+  const int keep = cfg->save_for_backward && ffn_tc_supported(*cfg) ? 1 : 0;
+  return router + stats + dispatch + ffn + combine + keep;
 }
 
 int32_t moe_backward_launch_count(const moe_config* cfg) {

@@ -70,17 +70,20 @@ struct WsLayout {
   size_t logits;              // [T][N] fp32 router logits
   size_t pre;                 // [R_max][2F] dtype: SwiGLU gate | up pre-activations
                               // (GELU: z in the first F columns); the backward pass
-                              // overwrites them in place with their gradients
+                              // overwrites them in place with their gradients. The
+                              // tensor-core path: [R_pad][2F], padded rows
   size_t count;               // [N] int32 assignments per expert
-  size_t dout;                // [R_max][d] dtype: expert output gradients
+  size_t dout;                // [R_pad][d] dtype: expert output gradients (tensor-core path:
+                              // padded rows, each expert's rows rounded up to 64)
+  size_t poff;                // [N+S+1] int32 padded row offsets
   size_t dg;                  // [T][K] fp32 gate gradients
   size_t dl;                  // [T][N] fp32 logit gradients
   size_t rpart;               // [rsplits][N][d + 1] fp32 router-gradient partials
   size_t bpart;               // [ceil(T/256)][N] fp32 partial column sums of dl (db_r)
   // tensor-core router gradients (bf16 layers with d % 256 == 0):
-  size_t r_ar;                // [T][3 NP] bf16: dl_hi | dl_lo | dl_hi
+  size_t r_ar;                // [Tp][3 NP] bf16: dl_hi | dl_lo | dl_hi (Tp = T rounded up to 64)
   size_t r_br;                // [3 NP][d] bf16: W_hi ; W_hi ; W_mid
-  size_t r_goff;              // [G + 3] int32 token-group offsets, then {0, T}
+  size_t r_goff;              // [2G + 6] int32 token-group offsets (A rows, x rows), then dx's
   size_t r_part;              // [G][2 NP][d] fp32 partial dW_r
   size_t total;
   int64_t a_max;
@@ -146,10 +149,14 @@ moe_status launch_ffn_simt(const moe_config& c, int64_t rows, const void* x_perm
 
 // Expert FFN on tcgen05 tensor cores (bf16, d % 256 == 0, F % 128 == 0).
 bool ffn_tc_supported(const moe_config& c);
+// pre (NULL or [padded rows][2F]) at rows poff[e] + r (the backward's padded
+// row space, each expert's rows rounded up to 64).
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w,
-                         void* h, float* o, void* pre, uint32_t* status, cudaStream_t s,
-                         int part);
+                         void* h, float* o, void* pre, const int32_t* poff, uint32_t* status,
+                         cudaStream_t s, int part);
+// poff[e] = sum over e' < e of the rows of e' rounded up to 64 (one warp).
+moe_status launch_pad_offsets(const int32_t* offsets, int G, int32_t* poff, cudaStream_t s);
 
 // Backward pass (backward.cu): every gradient, from the state moe_forward
 // kept in the workspace.
@@ -169,5 +176,7 @@ moe_status launch_backward(const moe_config& c, const WsLayout& L, void* ws, con
                            const float* w_r, const moe_expert_weights& w, const void* dy,
                            float z_coef, const moe_grads& g, uint32_t* status, cudaStream_t s);
 int backward_launch_count(const moe_config& c);
+bool ffn_bwd_tc_supported(const moe_config& c);
+int64_t ffn_bwd_pad_rows(const moe_config& c);
 
 }  // namespace moe

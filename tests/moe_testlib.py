@@ -31,6 +31,14 @@ GATE_TOL = 1e-5
 STAT_RTOL = 1e-5
 
 
+def stored_cf(cfg) -> float:
+    """The capacity factor as the layer stores it (moe_config carries a
+    float32), which is the value the oracle must be given: e.g. 0.9f is just
+    below 0.9, so floor(2 * 0.9f * 3000 / 4) = 1349 where the double 0.9 gives
+    1350."""
+    return float(np.float32(cfg.capacity_factor))
+
+
 def y_tolerance(dtype: str) -> float:
     return 1e-4 if dtype == "f32" else 2e-2
 
@@ -154,7 +162,7 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
     idx_gpu = gpu["idx"].numpy().astype(np.int64)
     n_near, n_diff = check_routing(key64, idx_gpu, K)
     ref = O.moe_forward(x, w_r, b_r, expert_reader(inp["experts"]), K=K,
-                        activation=cfg.activation, capacity_factor=cfg.capacity_factor,
+                        activation=cfg.activation, capacity_factor=stored_cf(cfg),
                         alpha=cfg.alpha, add_residual=cfg.add_residual, tokens=tokens,
                         idx_override=idx_gpu, gate_mode=cfg.gate_mode, select_bias=sb,
                         n_shared=cfg.n_shared)
@@ -169,7 +177,7 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
     assert abs(st["entropy"] - ref["entropy"]) <= STAT_RTOL * abs(ref["entropy"]) + 1e-6
     assert st["status"] == 0
     # dispatch: bit-exact
-    assert np.array_equal(st["kept"], ref["kept"])
+    assert np.array_equal(st["kept"], ref["kept"]), (st["kept"], ref["kept"])
     assert st["n_dropped"] == ref["n_dropped"]
     S, T = cfg.n_shared, cfg.T
     offs = gpu["offsets"].numpy()
@@ -354,7 +362,7 @@ def check_backward(cfg: moe.LayerConfig, inp: dict, dy, z_coef: float, *, tokens
     key64 = l64 if sb is None else l64 + O.f64(sb)[None, :]
     check_routing(key64, idx, K)
     ref = OG.moe_backward(x, w_r, b_r, expert_reader(inp["experts"]), dy.cpu(), K=K,
-                          activation=cfg.activation, capacity_factor=cfg.capacity_factor,
+                          activation=cfg.activation, capacity_factor=stored_cf(cfg),
                           alpha=cfg.alpha, z_coef=z_coef, add_residual=cfg.add_residual,
                           gate_mode=cfg.gate_mode, select_bias=sb, n_shared=cfg.n_shared,
                           idx_override=idx, tokens=tokens, experts=experts,

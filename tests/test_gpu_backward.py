@@ -44,6 +44,10 @@ CASES = {
                                     capacity_factor=0.5, add_residual=True), 0.0),
     # long per-expert reductions with ragged tails; 128-column tiles along F
     "bf16_many_rows_f384": (wl(T=3000, d=256, F=384, N=2, K=1, router_bias="uniform"), 0.0),
+    # backward products on CTA pairs (>= 512 rows per expert): skewed counts,
+    # drops, ragged padded tails
+    "bf16_pairs_capacity_skew": (wl(T=3000, d=512, F=512, N=4, K=2, capacity_factor=0.9,
+                                    router_bias="skew"), 0.0),
     # forward on CTA pairs (pre-activations kept by the pair kernel)
     "bf16_pair_forward_shared": (wl(T=2048, d=1024, F=2048, N=2, K=1, n_shared=1,
                                     capacity_factor=1.5, add_residual=True), 0.0),
