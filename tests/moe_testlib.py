@@ -251,13 +251,21 @@ def grad_rounding_bounds(cfg: moe.LayerConfig, inp: dict, dy, ref: dict) -> dict
     E_dxp_tok = np.zeros((len(tok), xs.shape[1]))
     E_dg = np.zeros((T, K))
     bounds = {"dw_gate": {}, "dw_up": {}, "dw_down": {}}
+    # rows to evaluate: every row of an expert whose weight gradient is
+    # compared, and the rows of the compared tokens (all tokens when the
+    # router gradients are compared, which need every gate gradient)
+    all_rows = "dw_r" in ref
+    wanted = set(ref["dw"])
     rows_of = {}
     for t in range(T):
         for k in range(K):
             if slot_of[t, k] >= 0:
-                rows_of.setdefault(int(idx[t, k]), []).append((t, k))
+                e = int(idx[t, k])
+                if all_rows or e in wanted or t in tok_pos:
+                    rows_of.setdefault(e, []).append((t, k))
     for s_ in range(S):
-        rows_of[N + s_] = [(t, -1) for t in range(T)]
+        ts = range(T) if (all_rows or N + s_ in wanted) else [int(t) for t in tok]
+        rows_of[N + s_] = [(t, -1) for t in ts]
     for e, rows in rows_of.items():
         ew = {kk: O.f64(v) for kk, v in reader(e).items() if v is not None}
         ts = [t for t, _ in rows]
@@ -299,15 +307,17 @@ def grad_rounding_bounds(cfg: moe.LayerConfig, inp: dict, dy, ref: dict) -> dict
             bounds.setdefault(k, {}).setdefault(e, np.zeros_like(v))
     w_r = O.f64(inp["w_r"])
     bounds["dx"] = E_dxp_tok + E_dl[tok] @ np.abs(w_r)
-    bounds["dw_r"] = E_dl.T @ np.abs(xs)
-    bounds["db_r"] = E_dl.sum(axis=0)
+    if all_rows:
+        bounds["dw_r"] = E_dl.T @ np.abs(xs)
+        bounds["db_r"] = E_dl.sum(axis=0)
     return bounds
 
 
-def run_backward(cfg: moe.LayerConfig, inp: dict, dy, z_coef: float):
+def run_backward(cfg: moe.LayerConfig, inp: dict, dy, z_coef: float, on_device: bool = False):
     """Forward (keeping state) then backward through the C ABI; returns the
-    host gradients, the GPU routing (from moe_route, the same kernels) and the
-    forward's y."""
+    gradients (host copies, or the device tensors with on_device), the GPU
+    routing (from moe_route, the same kernels), the forward's y and the
+    statistics."""
     cfg = moe.LayerConfig(**{**cfg.__dict__, "save_for_backward": True})
     layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
     y = layer.forward(inp["x"]).clone()
@@ -320,7 +330,7 @@ def run_backward(cfg: moe.LayerConfig, inp: dict, dy, z_coef: float):
     moe.moe_route(cfg, inp["x"], inp["w_r"], inp["b_r"], idx, gate, None,
                   moe.alloc_workspace(cfg))
     torch.cuda.synchronize()
-    out = {k: (None if v is None else v.cpu()) for k, v in g.items()}
+    out = dict(g) if on_device else {k: (None if v is None else v.cpu()) for k, v in g.items()}
     return out, idx.cpu().numpy().astype(np.int64), y.cpu(), st
 
 
@@ -352,7 +362,7 @@ def check_backward(cfg: moe.LayerConfig, inp: dict, dy, z_coef: float, *, tokens
     and expert weight gradients compared (None = all). fp32 layers: max |err|
     <= 1e-4 rms; bf16 (SwiGLU) layers: the per-element rounding bound of
     grad_rounding_bounds. Returns the ratios max |err| / rms per gradient."""
-    grads, idx, _, st = run_backward(cfg, inp, dy, z_coef)
+    grads, idx, _, st = run_backward(cfg, inp, dy, z_coef, on_device=True)
     assert st["status"] == 0
     K = cfg.top_k
     x, w_r = inp["x"].cpu(), inp["w_r"].cpu()
@@ -375,13 +385,15 @@ def check_backward(cfg: moe.LayerConfig, inp: dict, dy, z_coef: float, *, tokens
         lambda k, e=None: bnd[k] if e is None else bnd[k][e])
     ratios = {}
     tok = ref["tokens"]
-    ratios["dx"] = compare("dx", grads["dx"].numpy()[tok], ref["dx"], pick("dx"))
+    host = lambda t: t.cpu().numpy()  # copy only the compared slices off the device
+    ratios["dx"] = compare("dx", host(grads["dx"][torch.as_tensor(tok, device="cuda")]),
+                           ref["dx"], pick("dx"))
     if router_grads:
-        ratios["dw_r"] = compare("dw_r", grads["dw_r"].numpy(), ref["dw_r"], pick("dw_r"))
+        ratios["dw_r"] = compare("dw_r", host(grads["dw_r"]), ref["dw_r"], pick("dw_r"))
         if b_r is not None:
-            ratios["db_r"] = compare("db_r", grads["db_r"].numpy(), ref["db_r"], pick("db_r"))
+            ratios["db_r"] = compare("db_r", host(grads["db_r"]), ref["db_r"], pick("db_r"))
     for e, dw in ref["dw"].items():
         for k, v in dw.items():
-            r = compare(f"{k}[{e}]", grads[k].numpy()[e], v, pick(k, e))
+            r = compare(f"{k}[{e}]", host(grads[k][e]), v, pick(k, e))
             ratios[k] = max(ratios.get(k, 0.0), r)
     return ratios

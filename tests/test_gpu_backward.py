@@ -82,6 +82,29 @@ def test_backward_small(name):
     print(name, {k: f"{v:.2e}" for k, v in ratios.items()})
 
 
+# Full-size layers in the configuration the training bench times: dx on
+# sampled tokens (every assignment of each, including dropped ones), the
+# weight gradients of sampled experts (hot and cold), and the router
+# gradients where the oracle can afford every expert row (Switch, decode).
+FULL = {
+    "switch_skewed": dict(experts=[0, 37], router_grads=True),
+    "mixtral_decode": dict(experts=None, router_grads=True),
+    "mixtral_prefill": dict(experts=[], router_grads=False),
+    "deepseek_fine": dict(experts=[5, 200], router_grads=False),
+    "deepseek_shared": dict(experts=[17, 256], router_grads=False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
+def test_backward_full_size(name):
+    w = moe_inputs.WORKLOADS[name]
+    cfg, inp, dy = inputs(w)
+    rng = np.random.default_rng(11)
+    tokens = sorted(rng.choice(w.T, size=min(w.T, 40), replace=False).tolist())
+    ratios = L.check_backward(cfg, inp, dy, 1e-3, tokens=tokens, **FULL[name])
+    print(name, {k: f"{v:.2e}" for k, v in ratios.items()})
+
+
 def test_backward_deterministic():
     w, z = CASES["bf16_capacity_residual_z"]
     cfg, inp, dy = inputs(w)
