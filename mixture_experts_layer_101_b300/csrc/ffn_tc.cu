@@ -36,6 +36,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 
 namespace moe {
@@ -81,6 +82,10 @@ struct TcArgs {
                            // (gate | up) kept for the backward pass, row poff[e] + r for
                            // row r of expert e
   const int32_t* poff;     // [N+1] padded row offsets (with pre)
+  int ksplit;              // gate/up: reduction split in ksplit parts (1: none); with
+  float* part;             // ksplit > 1 the epilogue writes fp32 gate | up partials
+  int64_t rows_part;       // part[ks][row][2F] (rows_part rows per part) and
+                           // swiglu_combine_kernel applies SwiGLU
 };
 
 // The 32 gate and 32 up pre-activations of one row chunk, rounded to bf16, at
@@ -165,7 +170,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (e < N) {
         const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
         seg_off[e] = o0;
-        tiles = ((o1 - o0 + BM - 1) / BM) * args.n_tiles;
+        tiles = ((o1 - o0 + BM - 1) / BM) * args.n_tiles * args.ksplit;
       }
       local[j] = tiles;
       sum += tiles;
@@ -192,7 +197,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const uint32_t tmem_base = *tmem_slot;
   const int total = tile_start[N];
 
-  auto decode = [&](int tile, int& e, int& m, int& n) {
+  // tile -> expert e, row tile m, column tile n, reduction part ks (m fastest,
+  // then ks, then n: CTAs running together share the weight tile's rows)
+  auto decode = [&](int tile, int& e, int& m, int& n, int& ks) {
     int lo = 0, hi = N - 1;  // last expert whose first tile is <= tile
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -202,9 +209,14 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     e = lo;
     const int mt = (seg_off[e + 1] - seg_off[e] + BM - 1) / BM;
     const int local = tile - tile_start[e];
-    n = local / mt;
-    m = local - n * mt;
+    n = local / (mt * args.ksplit);
+    const int rem = local - n * mt * args.ksplit;
+    ks = rem / mt;
+    m = rem - ks * mt;
   };
+  // the 64-wide K steps of reduction part ks
+  auto kb_begin = [&](int ks) { return ks * KB / args.ksplit; };
+  auto kb_end = [&](int ks) { return (ks + 1) * KB / args.ksplit; };
   auto fail = [&]() {
     set_status(args.status, MOE_ERR_TIMEOUT);
     *abort_flag = 1;
@@ -216,8 +228,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t phase = 0, issued = 0, issued_parity = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      int e, m, n;
-      decode(tile, e, m, n);
+      int e, m, n, ks;
+      decode(tile, e, m, n, ks);
       const int row_a = seg_off[e] + m * BM;
       const int row_b = e * args.b_rows + n * Sh::OUT_COLS;
       // Only the expert's rows of this tile are fetched (smallest box that
@@ -226,7 +238,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int rows = min(BM, seg_off[e + 1] - row_a);
       const CUtensorMap* mapA = rows > 64 ? &tmA : (rows > 32 ? &tmA64 : (rows > 16 ? &tmA32 : &tmA16));
       const uint32_t a_bytes = static_cast<uint32_t>(rows > 64 ? 128 : (rows > 32 ? 64 : (rows > 16 ? 32 : 16))) * BK * 2;
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb = kb_begin(ks); kb < kb_end(ks); ++kb) {
         if (!mbar_wait(bar_empty(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
           ok = false;
           break;
@@ -260,13 +272,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued_any = false;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, m, n, ks;
+      decode(tile, e, m, n, ks);
+      const int kb0 = kb_begin(ks), kb1 = kb_end(ks);
       if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Sh::ACC);
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(bar_full(stage), phase, kWaitLimitNs, abort_flag)) {
           ok = false;
           break;
@@ -276,7 +291,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           mma_bf16(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32), sdesc_kmajor_sw128(b0 + kk * 32),
-                   Sh::IDESC, (kb | kk) != 0 ? 1u : 0u);
+                   Sh::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
         issued_any = true;
         mma_commit(bar_empty(stage));
         if (++stage == STAGES) {
@@ -302,8 +317,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int e, m, n;
-      decode(tile, e, m, n);
+      int e, m, n, ks;
+      decode(tile, e, m, n, ks);
       const int cnt = seg_off[e + 1] - seg_off[e];
       bool ok = mbar_wait(bar_tfull(acc), acc_phase, kWaitLimitNs, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
@@ -317,7 +332,29 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const size_t grow = static_cast<size_t>(seg_off[e]) + static_cast<size_t>(r);
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * Sh::ACC) +
                              (static_cast<uint32_t>(q * 32) << 16);
-      if (MODE == 0) {
+      if (MODE == 0 && args.ksplit > 1) {
+        // reduction part ks: fp32 gate | up partials of this row
+        float* pg = args.part + (static_cast<size_t>(ks) * args.rows_part + grow) * 2 * args.ldo +
+                    n * Sh::OUT_COLS;
+#pragma unroll 1
+        for (int c = 0; c < BNH / 32; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + BNH + c * 32, u);
+          tmem_ld_wait();
+          if (valid) {
+            float4* dg = reinterpret_cast<float4*>(pg + c * 32);
+            float4* du = reinterpret_cast<float4*>(pg + args.ldo + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              dg[j] = make_float4(__uint_as_float(g[4 * j]), __uint_as_float(g[4 * j + 1]),
+                                  __uint_as_float(g[4 * j + 2]), __uint_as_float(g[4 * j + 3]));
+              du[j] = make_float4(__uint_as_float(u[4 * j]), __uint_as_float(u[4 * j + 1]),
+                                  __uint_as_float(u[4 * j + 2]), __uint_as_float(u[4 * j + 3]));
+            }
+          }
+        }
+      } else if (MODE == 0) {
         __nv_bfloat16* out =
             static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo + n * Sh::OUT_COLS;
 #pragma unroll 1
@@ -685,6 +722,51 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
+// Gate/up with a split reduction: h[r][f] = silu(g) * u with g, u the sums of
+// the parts' fp32 partials in ascending part order (the same SwiGLU as the
+// GEMM epilogue); with pre, (g, u) rounded to bf16 are kept at padded row
+// poff[e] + (r - offsets[e]). Block r handles row r (rows past offsets[E]
+// have no data and return).
+__global__ void __launch_bounds__(256)
+swiglu_combine_kernel(const float* __restrict__ part, int ksplit, int64_t rows_part,
+                      const int32_t* __restrict__ offsets, int E, int F,
+                      __nv_bfloat16* __restrict__ h, __nv_bfloat16* __restrict__ pre,
+                      const int32_t* __restrict__ poff) {
+  const int r = blockIdx.x;
+  if (r >= offsets[E]) return;
+  int prow = 0;
+  if (pre != nullptr) {
+    int lo = 0, hi = E - 1;  // the expert whose rows hold r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (offsets[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    prow = poff[lo] + (r - offsets[lo]);
+  }
+  for (int f = threadIdx.x * 2; f < F; f += blockDim.x * 2) {
+    float2 g = make_float2(0.f, 0.f), u = make_float2(0.f, 0.f);
+    for (int ks = 0; ks < ksplit; ++ks) {
+      const float* row = part + (static_cast<size_t>(ks) * rows_part + r) * 2 * F;
+      const float2 pg = *reinterpret_cast<const float2*>(row + f);
+      const float2 pu = *reinterpret_cast<const float2*>(row + F + f);
+      g.x += pg.x;
+      g.y += pg.y;
+      u.x += pu.x;
+      u.y += pu.y;
+    }
+    const float h0 = g.x / (1.f + __expf(-g.x)) * u.x;
+    const float h1 = g.y / (1.f + __expf(-g.y)) * u.y;
+    *reinterpret_cast<__nv_bfloat162*>(h + static_cast<size_t>(r) * F + f) =
+        __floats2bfloat162_rn(h0, h1);
+    if (pre != nullptr) {
+      __nv_bfloat16* pr = pre + static_cast<size_t>(prow) * 2 * F;
+      *reinterpret_cast<__nv_bfloat162*>(pr + f) = __floats2bfloat162_rn(g.x, g.y);
+      *reinterpret_cast<__nv_bfloat162*>(pr + F + f) = __floats2bfloat162_rn(u.x, u.y);
+    }
+  }
+}
+
 // ---- host side ---------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -769,6 +851,35 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 
 }  // namespace
 
+// Reduction split of the one-CTA gate/up GEMM for batches with about one row
+// tile per expert (decode): the persistent grid then deals E_active x F/128
+// weight-streaming tiles to the SMs, and the last partial wave can cost a
+// whole tile time (8 x 112 tiles on 148 SMs: 6.05 waves take 7). Splitting
+// each tile's reduction in s parts makes the units s times smaller; s is the
+// smallest in 1..8 whose last wave wastes at most 4 % (experts assumed all
+// active, each with one row tile). Returns 1 otherwise.
+int gate_up_ksplit(const moe_config& c, int64_t rows) {
+  const int E = c.n_experts + c.n_shared;
+  const int KB = c.d_model / BK;
+  if (c.dtype != MOE_BF16 || rows > static_cast<int64_t>(E) * BM || KB < 16) return 1;
+  const int64_t active = rows < E ? rows : E;
+  const int64_t tiles = active * (c.d_ff / 128);
+  const int sms = sm_count();
+  int best = 1;
+  double best_waste = 1e9;
+  for (int sp = 1; sp <= 8 && KB / sp >= 4; ++sp) {
+    const double units = static_cast<double>(tiles) * sp;
+    const double waves = units / sms;
+    const double waste = std::ceil(waves) / waves - 1.0;
+    if (waste < best_waste - 1e-9) {
+      best_waste = waste;
+      best = sp;
+    }
+    if (waste <= 0.04) break;
+  }
+  return best;
+}
+
 bool ffn_tc_supported(const moe_config& c) {
   return c.dtype == MOE_BF16 && c.activation == MOE_SWIGLU && c.d_model % 256 == 0 &&
          c.d_ff % 128 == 0 && c.n_experts + c.n_shared <= MAX_EXPERTS;
@@ -776,8 +887,8 @@ bool ffn_tc_supported(const moe_config& c) {
 
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w, void* h, float* o,
-                         void* pre, const int32_t* poff, uint32_t* status, cudaStream_t s,
-                         int part) {
+                         void* pre, const int32_t* poff, float* gu_part, uint32_t* status,
+                         cudaStream_t s, int part) {
   if (rows == 0) return MOE_OK;
   const int E = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
   const bool pairs1 = use_pairs(c, rows, d);  // gate/up: reduction over d
@@ -792,7 +903,8 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
         !make_map(&mg, w.w_gate, static_cast<uint64_t>(E) * F, d, 128) ||
         !make_map(&mu, w.w_up, static_cast<uint64_t>(E) * F, d, 128))
       return MOE_ERR_CUDA;
-    TcArgs a1{offsets, E, d, F / 128, F, h, F, status, pre, poff};
+    const int ksplit = pairs1 ? 1 : gate_up_ksplit(c, rows);
+    TcArgs a1{offsets, E, d, F / 128, F, h, F, status, pre, poff, ksplit, gu_part, rows};
     if (pairs1) {
       if (launch_pair<0>(mx, mg, mu, a1, ptiles * (F / 128), s) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -801,10 +913,16 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
       if (!make_map(&mx64, x_perm, rows, d, 64) || !make_map(&mx32, x_perm, rows, d, 32) ||
           !make_map(&mx16, x_perm, rows, d, 16))
         return MOE_ERR_CUDA;
-      const int64_t t1 = mtiles * (F / 128);
+      const int64_t t1 = mtiles * (F / 128) * ksplit;
       grouped_gemm_tc<0, 128><<<static_cast<unsigned>(t1 < sms ? t1 : sms), kThreads,
                                 TcShape<0, 128>::SMEM, s>>>(mx, mg, mu, mx64, mx32, mx16, a1);
       if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+      if (ksplit > 1) {
+        swiglu_combine_kernel<<<static_cast<unsigned>(rows), 256, 0, s>>>(
+            gu_part, ksplit, rows, offsets, E, F, static_cast<__nv_bfloat16*>(h),
+            static_cast<__nv_bfloat16*>(pre), poff);
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+      }
     }
   }
   if (part & 2) {
@@ -812,7 +930,7 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
     if (!make_map(&mh, h, rows, F, 128) ||
         !make_map(&md, w.w_down, static_cast<uint64_t>(E) * d, F, pairs2 ? 128 : 256))
       return MOE_ERR_CUDA;
-    TcArgs a2{offsets, E, F, d / 256, d, o, d, status, nullptr, nullptr};
+    TcArgs a2{offsets, E, F, d / 256, d, o, d, status, nullptr, nullptr, 1, nullptr, rows};
     if (pairs2) {
       if (launch_pair<1>(mh, md, md, a2, ptiles * (d / 256), s) != cudaSuccess)
         return MOE_ERR_CUDA;

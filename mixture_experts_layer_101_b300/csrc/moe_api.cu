@@ -102,6 +102,8 @@ WsLayout ws_layout(const moe_config* c) {
   L.x_perm = take(A * d * es);
   L.h = take(A * F * es);
   L.o = take(A * d * 4);
+  const int ks = ffn_tc_supported(*c) ? gate_up_ksplit(*c, static_cast<int64_t>(A)) : 1;
+  L.gu_part = take(ks > 1 ? static_cast<size_t>(ks) * A * 2 * F * 4 : 0);
   const bool bw = c->save_for_backward != 0;
   // router-gradient K splits: about 1024 tokens each, at most 32
   L.rsplits = bw ? static_cast<int>(std::min<size_t>(32, std::max<size_t>(1, T / 1024))) : 0;
@@ -205,7 +207,8 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
   for (int part = 1; part <= 2; ++part) {
     const int64_t rows = rows_max_of(c);
     const moe_status r =
-        tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, pre, poff, status, s, part)
+        tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, pre, poff,
+                           reinterpret_cast<float*>(at(ws, L.gu_part)), status, s, part)
            : launch_ffn_simt(*c, rows, x_perm, offsets, *w, h, o, pre, s, part);
     if (r != MOE_OK) return r;
     if (traced) trace(2 + part, s);
@@ -238,7 +241,8 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   const int router = rp.use ? (rp.fused ? 2 : 3) : 1;
   const int stats = 2;                                  // per-expert reduction, L_aux
   const int dispatch = 4;                               // histogram, scan, permute, gather
-  const int ffn = 2;                                    // gate/up, down
+  // gate/up (+ the SwiGLU of a split reduction), down
+  const int ffn = 2 + (ffn_tc_supported(*cfg) && gate_up_ksplit(*cfg, rows_max_of(cfg)) > 1 ? 1 : 0);
   const int combine = 1;
   // keeping the pre-activations for the tensor-core backward: their padded offsets
   const int keep = cfg->save_for_backward && ffn_tc_supported(*cfg) ? 1 : 0;

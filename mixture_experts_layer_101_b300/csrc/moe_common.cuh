@@ -66,6 +66,7 @@ struct WsLayout {
   size_t h;                   // [A_max][F] dtype
   size_t o;                   // [A_max][d] fp32 (moe_forward only); the backward
                               // pass reuses it for the expert input gradients
+  size_t gu_part;             // [ksplit][R_max][2F] fp32 split gate/up partials (decode)
   // save_for_backward only (size 0 otherwise):
   size_t logits;              // [T][N] fp32 router logits
   size_t pre;                 // [R_max][2F] dtype: SwiGLU gate | up pre-activations
@@ -150,11 +151,14 @@ moe_status launch_ffn_simt(const moe_config& c, int64_t rows, const void* x_perm
 // Expert FFN on tcgen05 tensor cores (bf16, d % 256 == 0, F % 128 == 0).
 bool ffn_tc_supported(const moe_config& c);
 // pre (NULL or [padded rows][2F]) at rows poff[e] + r (the backward's padded
-// row space, each expert's rows rounded up to 64).
+// row space, each expert's rows rounded up to 64). gu_part: fp32 partials
+// [gate_up_ksplit][rows][2F] of a split gate/up reduction (decode-sized
+// batches; NULL when gate_up_ksplit(c, rows) == 1).
+int gate_up_ksplit(const moe_config& c, int64_t rows);
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w,
-                         void* h, float* o, void* pre, const int32_t* poff, uint32_t* status,
-                         cudaStream_t s, int part);
+                         void* h, float* o, void* pre, const int32_t* poff, float* gu_part,
+                         uint32_t* status, cudaStream_t s, int part);
 // poff[e] = sum over e' < e of the rows of e' rounded up to 64 (one warp).
 moe_status launch_pad_offsets(const int32_t* offsets, int G, int32_t* poff, cudaStream_t s);
 

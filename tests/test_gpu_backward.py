@@ -48,6 +48,9 @@ CASES = {
     # drops, ragged padded tails
     "bf16_pairs_capacity_skew": (wl(T=3000, d=512, F=512, N=4, K=2, capacity_factor=0.9,
                                     router_bias="skew"), 0.0),
+    # decode-sized batch: the forward's split gate/up reduction keeps the
+    # pre-activations through its combining kernel
+    "bf16_decode_split_k": (wl(T=24, d=1024, F=256, N=8, K=2), 0.0),
     # forward on CTA pairs (pre-activations kept by the pair kernel)
     "bf16_pair_forward_shared": (wl(T=2048, d=1024, F=2048, N=2, K=1, n_shared=1,
                                     capacity_factor=1.5, add_residual=True), 0.0),

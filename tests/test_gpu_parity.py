@@ -73,6 +73,10 @@ SMALL = {
     "fused_router_switch_gate": wl(T=2000, d=64, F=64, N=64, K=1, gate_mode="softmax",
                                    capacity_factor=1.25, add_residual=True, router_bias="skew"),
     "fused_router_chunks": wl(T=19500, d=256, F=64, N=40, K=2, router_bias="uniform"),
+    # decode-sized batch (about one row tile per expert): the gate/up reduction
+    # is split in parts whose fp32 partials a second kernel sums before SwiGLU
+    "tc_decode_split_k": wl(T=24, d=1024, F=256, N=8, K=2),
+    "tc_decode_split_k_shared": wl(T=9, d=2048, F=128, N=4, K=1, n_shared=1),
     # CUDA-core path: fp32, GELU, or shapes the tensor-core kernel does not tile
     "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
     "simt_gelu_nobias": wl(T=90, d=64, F=96, N=4, K=2, dtype="f32", activation="gelu",
