@@ -670,8 +670,9 @@ def run_train(args, world, rank):
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
                     "h2d_bytes_per_step": 2 * w.T * w.d * es,
                     "d2h_bytes_per_step": w.T * w.d * 4 + 4},
-            "gpu_launches": (moe.forward_launch_count(cfg) + moe.backward_launch_count(cfg))
-            * args.steps,
+            # moe_backward_launch_count counts the router-bias gradient (2 kernels)
+            "gpu_launches": (moe.forward_launch_count(cfg) + moe.backward_launch_count(cfg)
+                             - (0 if b_r is not None else 2)) * args.steps,
             "clocks": ck,
             "wall_s_timed_region": round(wall, 4),
         }

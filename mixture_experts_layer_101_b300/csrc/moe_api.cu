@@ -82,7 +82,7 @@ WsLayout ws_layout(const moe_config* c) {
   const size_t T = static_cast<size_t>(c->T), K = c->top_k, N = c->n_experts;
   const size_t d = c->d_model, F = c->d_ff, es = dtype_size(c);
   L.a_max = a_max_of(c);
-  L.nblk_r = static_cast<int>((T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock);
+  L.nblk_r = static_cast<int>((T + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock);
   L.nblk_d = static_cast<int>((T + kDispatchTokensPerBlock - 1) / kDispatchTokensPerBlock);
   const size_t nr = L.nblk_r > 0 ? L.nblk_r : 1, nd = L.nblk_d > 0 ? L.nblk_d : 1;
   const size_t A = static_cast<size_t>(rows_max_of(c));  // routed + shared rows

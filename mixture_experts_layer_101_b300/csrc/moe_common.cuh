@@ -50,12 +50,14 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
 // ---- workspace layout ------------------------------------------------------
 // Every region is 256-byte aligned. The same layout serves every entry point;
 // moe_workspace_size() returns its total.
-constexpr int kRouterTokensPerBlock = 32;   // tokens per router block
+constexpr int kRouterTokensPerBlock = 32;   // tokens per CUDA-core router block
+constexpr int kTopkTokensPerBlock = 8;      // tokens per top-K block (one per warp)
 constexpr int kDispatchTokensPerBlock = 256; // tokens per dispatch block
 
 struct WsLayout {
   size_t idx, gate;           // [T][K] int32 / fp32 (moe_forward only)
-  size_t psum, pcnt;          // router partials [N+2][nblk_r], [N][nblk_r] (expert-major)
+  size_t psum, pcnt;          // router partials [N+2][nblk_r], [N][nblk_r] (expert-major);
+                              // nblk_r = ceil(T / kTopkTokensPerBlock) covers every router
   size_t w3, part;            // tensor-core router: W_r split [3][NP][d] bf16,
                               // partial logits [S][T][NP] fp32
   size_t ghist, gbase;        // dispatch histograms [K][nblk_d][N]

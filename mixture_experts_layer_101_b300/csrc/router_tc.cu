@@ -439,7 +439,8 @@ router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 }
 
 // Warp per token: logits = sum over the K splits in order + bias; then the
-// shared selection code. 32 tokens per 256-thread block.
+// shared selection code. One token per warp, 8 per 256-thread block (enough
+// blocks to fill the GPU at a few thousand tokens).
 template <int NJ>
 __global__ void __launch_bounds__(256)
 router_topk_kernel(const float* __restrict__ part, int S, int NP, const float* __restrict__ b_r,
@@ -457,8 +458,8 @@ router_topk_kernel(const float* __restrict__ part, int S, int NP, const float* _
 #pragma unroll
   for (int j = 0; j < NJ; ++j) pacc[j] = 0.f;
   float zacc = 0.f, hacc = 0.f;
-  const int t0 = blockIdx.x * kRouterTokensPerBlock;
-  for (int tl = warp; tl < kRouterTokensPerBlock; tl += kSelectWarps) {
+  const int t0 = blockIdx.x * kTopkTokensPerBlock;
+  for (int tl = warp; tl < kTopkTokensPerBlock; tl += kSelectWarps) {
     const int t = t0 + tl;
     if (t >= T) break;
     float v[NJ];
@@ -546,7 +547,7 @@ RouterTcPlan router_tc_plan(const moe_config& c) {
   // one split and one expert tile: the GEMM epilogue holds whole tokens
   p.fused = p.S == 1 && p.NP == p.NPT;
   p.stat_blocks = p.fused ? (c.T + BM - 1) / BM
-                          : (c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+                          : (c.T + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock;
   return p;
 }
 
@@ -575,7 +576,7 @@ moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const vo
   else if (p.NPT == 64) e = launch_gemm<64, false>(mx, mw, a, grid, s);
   else e = launch_gemm<32, false>(mx, mw, a, grid, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+  const int nblk = (T + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock;
 #define MOE_TOPK(NJ)                                                                           \
   router_topk_kernel<NJ><<<nblk, 256, 0, s>>>(part, p.S, p.NP, b_r, c.select_bias, c.gate_mode, \
                                               T, N, c.top_k, idx, gate, psum, pcnt, status,    \
