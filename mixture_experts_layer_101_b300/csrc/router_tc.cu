@@ -156,11 +156,16 @@ __device__ __forceinline__ void fused_select(float (&v)[NPT], const GemmArgs& a,
   for (int i = 0; i < (NPT + 31) / 32; ++i) taken[i] = 0u;
   int sel_e[8];
   float sel_u[8];
+  // The rank loop stays rolled (sel_* then live in local memory): unrolled
+  // eight times over NPT experts, the epilogue's code outgrows the
+  // instruction cache.
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // unrolled: constant indices keep sel_* in registers
+  for (int k = 0; k < 8; ++k) {
     sel_e[k] = 0;
     sel_u[k] = -INFINITY;
-    if (k >= K) continue;
+  }
+#pragma unroll 1
+  for (int k = 0; k < K; ++k) {
     float bv = -INFINITY, bu = -INFINITY;
     int be = -1;
 #pragma unroll
