@@ -37,8 +37,22 @@ combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_of,
     s_slot[tt][k] = t < T ? slot_of[static_cast<size_t>(t) * KS + k] : -1;
     s_gate[tt][k] = (t < T && k < K) ? gate[static_cast<size_t>(t) * K + k] : 1.f;
   }
+  // The residual rows do not depend on the routing: the first columns' loads
+  // go out before the barrier, overlapping the slot lookups.
+  float4 xr[TPB];
+  auto load_residual = [&](int c) {
+#pragma unroll
+    for (int tt = 0; tt < TPB; ++tt) {
+      const int t = t0 + tt;
+      xr[tt] = (add_residual && t < T) ? load4(x + static_cast<size_t>(t) * d + c)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  const int c0 = threadIdx.x * 4;
+  if (c0 < d) load_residual(c0);
   __syncthreads();
-  for (int c = threadIdx.x * 4; c < d; c += kThreads * 4) {
+  for (int c = c0; c < d; c += kThreads * 4) {
+    if (c != c0) load_residual(c);
     float4 acc[TPB];
 #pragma unroll
     for (int tt = 0; tt < TPB; ++tt) acc[tt] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -61,11 +75,10 @@ combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_of,
       const int t = t0 + tt;
       if (t >= T) break;
       if (add_residual) {
-        const float4 xv = load4(x + static_cast<size_t>(t) * d + c);
-        acc[tt].x += xv.x;
-        acc[tt].y += xv.y;
-        acc[tt].z += xv.z;
-        acc[tt].w += xv.w;
+        acc[tt].x += xr[tt].x;
+        acc[tt].y += xr[tt].y;
+        acc[tt].z += xr[tt].z;
+        acc[tt].w += xr[tt].w;
       }
       store4(y + static_cast<size_t>(t) * d + c, acc[tt]);
     }

@@ -41,35 +41,73 @@ dispatch_hist_kernel(const int32_t* __restrict__ idx, int T, int K, int N,
   for (int e = threadIdx.x; e < N; e += kThreads) out[e] = hist[e];
 }
 
-// One block. Thread e scans its expert's column over the K*nb (k, b) blocks
-// in visiting order; then the kept counts are scanned over experts.
-__global__ void __launch_bounds__(256)
+// One block. Thread (g, e) = (tid / N, tid % N) owns the g-th of
+// G = kScanThreads / N runs of consecutive (k, b) blocks in expert e's
+// column: it sums its run, then writes the column's exclusive prefix over
+// its run starting from the totals of the runs before it (all integer, so
+// the result does not depend on the split). Warp 0 then scans the kept
+// counts over the experts.
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
 dispatch_scan_kernel(const int32_t* __restrict__ ghist, int nq, int N, int32_t C, int S, int T,
                      int32_t* __restrict__ gbase, int32_t* __restrict__ offsets,
                      int32_t* count, int32_t* kept_out, int32_t* n_dropped) {
+  __shared__ int32_t run_sum[kScanThreads];
   __shared__ int32_t kept[256], cnt[256];
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+  const int tid = threadIdx.x;
+  const int G = kScanThreads / N;  // N <= 256, so G >= 4
+  const int g = tid / N, e = tid - g * N;
+  const bool active = g < G;
+  const int per = (nq + G - 1) / G;
+  const int q0 = min(nq, g * per), q1 = min(nq, q0 + per);
+  int32_t sum = 0;
+  if (active)
+    for (int q = q0; q < q1; ++q) sum += ghist[static_cast<size_t>(q) * N + e];
+  run_sum[tid] = sum;
+  __syncthreads();
+  if (active) {
     int32_t run = 0;
-    for (int q = 0; q < nq; ++q) {
+    for (int h = 0; h < g; ++h) run += run_sum[h * N + e];
+    for (int q = q0; q < q1; ++q) {
       gbase[static_cast<size_t>(q) * N + e] = run;
       run += ghist[static_cast<size_t>(q) * N + e];
     }
-    cnt[e] = run;
-    kept[e] = run < C ? run : C;
-    if (count) count[e] = run;
-    if (kept_out) kept_out[e] = kept[e];
+    if (g == G - 1) {  // the last run ends the column: run is the expert's total
+      cnt[e] = run;
+      kept[e] = run < C ? run : C;
+      if (count) count[e] = run;
+      if (kept_out) kept_out[e] = kept[e];
+    }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t off = 0, dropped = 0;
-    for (int e = 0; e < N; ++e) {
-      offsets[e] = off;
-      off += kept[e];
-      dropped += cnt[e] - kept[e];
+  if (tid < 32) {
+    const int per_lane = (N + 31) / 32;
+    const int e0 = min(N, tid * per_lane), e1 = min(N, e0 + per_lane);
+    int32_t ks = 0, ds = 0;
+    for (int i = e0; i < e1; ++i) {
+      ks += kept[i];
+      ds += cnt[i] - kept[i];
     }
-    offsets[N] = off;
-    for (int s = 0; s < S; ++s) offsets[N + s + 1] = off + (s + 1) * T;  // shared experts
-    if (n_dropped) *n_dropped = dropped;
+    int32_t inc = ks;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (tid >= o) inc += v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ds += __shfl_xor_sync(0xffffffffu, ds, o);
+    int32_t off = inc - ks;
+    for (int i = e0; i < e1; ++i) {
+      offsets[i] = off;
+      off += kept[i];
+    }
+    const int32_t total = __shfl_sync(0xffffffffu, inc, 31);
+    if (tid == 0) {
+      offsets[N] = total;
+      for (int s2 = 0; s2 < S; ++s2) offsets[N + s2 + 1] = total + (s2 + 1) * T;  // shared experts
+      if (n_dropped) *n_dropped = ds;
+    }
   }
 }
 
@@ -155,10 +193,9 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
     dispatch_hist_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, ghist, status);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(ghist, c.T > 0 ? K * nb : 0, N, C, c.n_shared, c.T,
-                                         gbase, offsets,
-                                         st ? st->count : nullptr, st ? st->kept : nullptr,
-                                         st ? st->n_dropped : nullptr);
+  dispatch_scan_kernel<<<1, kScanThreads, 0, s>>>(
+      ghist, c.T > 0 ? K * nb : 0, N, C, c.n_shared, c.T, gbase, offsets,
+      st ? st->count : nullptr, st ? st->kept : nullptr, st ? st->n_dropped : nullptr);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   if (c.T > 0) {
     dispatch_permute_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, c.n_shared, C, gbase,
