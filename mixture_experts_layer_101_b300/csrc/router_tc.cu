@@ -100,17 +100,22 @@ struct GemmArgs {
 // Scratch in the drained stage buffers: p[128][NPT + 1] (the block's softmax
 // rows; the odd row pitch keeps both the row writes and the column reads free
 // of bank conflicts), zh[2][128] (per-token squared log-sum-exp and entropy),
-// cnt[NPT] (assignment counts).
+// cnt[NPT] (assignment counts), bias[NPT] and sbias[NPT] (router and
+// selection biases).
 template <int NPT>
 struct FusedScratch {
   float* p;
   float* zh;
   int32_t* cnt;
+  float* bias;   // b_r (0 where absent), read by every token's selection
+  float* sbias;  // selection bias (0 where absent)
   __device__ explicit FusedScratch(uint8_t* base)
       : p(reinterpret_cast<float*>(base)),
         zh(p + 128 * (NPT + 1)),
-        cnt(reinterpret_cast<int32_t*>(zh + 256)) {}
-  static constexpr int BYTES = (128 * (NPT + 1) + 256 + NPT) * 4;
+        cnt(reinterpret_cast<int32_t*>(zh + 256)),
+        bias(reinterpret_cast<float*>(cnt + NPT)),
+        sbias(bias + NPT) {}
+  static constexpr int BYTES = (128 * (NPT + 1) + 256 + 3 * NPT) * 4;
 };
 
 // One token per thread: v holds the token's NPT accumulated logits (entries
@@ -138,7 +143,7 @@ __device__ __forceinline__ void fused_select(float (&v)[NPT], const GemmArgs& a,
 #pragma unroll
   for (int e = 0; e < NPT; ++e) {
     if (e < N) {
-      if (a.b_r != nullptr) v[e] += a.b_r[e];
+      if (a.b_r != nullptr) v[e] += sc.bias[e];
       if (!isfinite(v[e])) bad = true;
       mx = fmaxf(mx, v[e]);
     }
@@ -172,7 +177,7 @@ __device__ __forceinline__ void fused_select(float (&v)[NPT], const GemmArgs& a,
     for (int e = 0; e < NPT; ++e) {
       if (e >= N || ((taken[e >> 5] >> (e & 31)) & 1u)) continue;
       const float u = isnan(v[e]) ? -INFINITY : v[e];
-      const float key = a.sel_bias != nullptr ? u + a.sel_bias[e] : u;
+      const float key = a.sel_bias != nullptr ? u + sc.sbias[e] : u;
       if (be < 0 || key > bv) {
         bv = key;
         be = e;
@@ -427,7 +432,11 @@ router_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       if (!ok && lane == 0) *epi_fail = 1;
       epilogue_bar();
       const bool all_ok = *epi_fail == 0;
-      if (all_ok && row < NPT) sc.cnt[row] = 0;
+      if (all_ok && row < NPT) {  // staged once here instead of NPT global loads per token
+        sc.cnt[row] = 0;
+        sc.bias[row] = (args.b_r != nullptr && row < args.N) ? args.b_r[row] : 0.f;
+        sc.sbias[row] = (args.sel_bias != nullptr && row < args.N) ? args.sel_bias[row] : 0.f;
+      }
       epilogue_bar();
       if (all_ok) fused_select<NPT>(run, args, m * BM + row, row, sc);
       epilogue_bar();
