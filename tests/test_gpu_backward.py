@@ -48,6 +48,9 @@ CASES = {
     # drops, ragged padded tails
     "bf16_pairs_capacity_skew": (wl(T=3000, d=512, F=512, N=4, K=2, capacity_factor=0.9,
                                     router_bias="skew"), 0.0),
+    # forward GEMMs as CTA pairs, expert tails of 244 241 3 24 rows past whole
+    # 256-row pair tiles
+    "bf16_pair_tails_mixed": (wl(T=2048, d=1024, F=1024, N=4, K=2, router_bias="uniform"), 0.0),
     # decode-sized batch: the forward's split gate/up reduction keeps the
     # pre-activations through its combining kernel
     "bf16_decode_split_k": (wl(T=24, d=1024, F=256, N=8, K=2), 0.0),

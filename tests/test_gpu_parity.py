@@ -44,11 +44,19 @@ SMALL = {
     "tc_many_tiles_capacity": wl(T=3000, d=512, F=128, N=4, K=1, capacity_factor=1.1,
                             router_bias="skew", add_residual=True),
     "tc_many_tiles_uneven": wl(T=2600, d=256, F=384, N=3, K=2, router_bias="skew"),
-    # CTA pairs (several tiles per expert and a reduction of >= 2048): both
-    # GEMMs in pairs; gate/up on one CTA per tile and down in pairs
+    # CTA pairs (several tiles per expert and a reduction of >= 1024): both
+    # GEMMs in pairs
     "tc_pairs_both": wl(T=1500, d=2048, F=2048, N=2, K=2),
     "tc_pairs_down_only": wl(T=2048, d=1024, F=2048, N=2, K=1, n_shared=1,
                              capacity_factor=1.5, add_residual=True),
+    # CTA pairs with expert tails on both sides of 128 rows (a last pair tile
+    # whose odd CTA holds no rows, or some) and exact multiples of 256 under a
+    # capacity (expert counts 1012 1009 1027 1048; the same capped at 1024;
+    # 1435 1415 1407 1453 245 189)
+    "tc_pair_tails_mixed": wl(T=2048, d=1024, F=1024, N=4, K=2, router_bias="uniform"),
+    "tc_pair_tails_exact": wl(T=2048, d=1024, F=1024, N=4, K=2, router_bias="uniform",
+                              capacity_factor=1.0, add_residual=True),
+    "tc_pair_tails_k3": wl(T=2048, d=1024, F=1024, N=6, K=3, router_bias="skew"),
     # enough tiles for the wide (128+128 column) gate/up tile of the one-CTA kernel
     "tc_wide_tiles": wl(T=4096, d=256, F=1280, N=64, K=2),
     # gate variants: full-softmax (Switch) gates, top-K selection bias
