@@ -111,11 +111,14 @@ def _uniform(shape, bound, gen, device):
     return (torch.rand(shape, generator=gen, device=device, dtype=torch.float32) * 2 - 1) * bound
 
 
-def make_x(w: MoEWorkload, T: int | None = None) -> torch.Tensor:
-    """x [T][d] on the CPU, in the storage dtype."""
+def make_x(w: MoEWorkload, T: int | None = None, device="cpu") -> torch.Tensor:
+    """x [T][d] in the storage dtype, N(0, 1), seed 0, drawn on `device` (the
+    CPU and CUDA generators give different numbers for the same seed: the
+    very large cases draw on the GPU, and the oracle then reads x back)."""
     T = w.T if T is None else T
-    g = _gen(X_SEED, "cpu")
-    return torch.randn((T, w.d), generator=g, dtype=torch.float32).to(w.torch_dtype)
+    g = _gen(X_SEED, device)
+    return torch.randn((T, w.d), generator=g, device=device,
+                       dtype=torch.float32).to(w.torch_dtype)
 
 
 def make_dy(w: MoEWorkload, T: int | None = None) -> torch.Tensor:
