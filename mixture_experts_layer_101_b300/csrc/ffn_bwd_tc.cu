@@ -602,9 +602,10 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
 // upper bound: rows of the workspace, before capacity) average at least 1024,
 // i.e. reductions of 16 or more 64-row steps per tile: there they are limited
 // by the bytes each SM loads per MMA cycle (measured on the Mixtral-shaped
-// layer: 1.08 -> 0.87 ms and 2.12 -> 1.70 ms). The input-gradient products
-// measured 2-6 % slower on pairs (their epilogue, not their loads, sets the
-// pace), and with ~200 rows per expert (the Switch-shaped layer) pairs lose.
+// layer: 1.08 -> 0.87 ms and 2.12 -> 1.70 ms); with ~200 rows per expert (the
+// Switch-shaped layer) pairs lose. The SwiGLU-derivative input gradient takes
+// pairs from 512 rows per expert and a reduction over d >= 1024 (measured:
+// Switch-shaped 0.277 -> 0.258 ms, Mixtral-shaped 0.96-0.99 -> 0.92-0.94 ms).
 bool use_pairs(int E, int64_t rows) { return rows >= static_cast<int64_t>(E) * 1024; }
 
 }  // namespace
@@ -651,7 +652,11 @@ moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, int64_t rows_pad
   {
     BwArgs a{poff, offsets, E, d / BK, d / BK, d, F / (f256 ? 256 : 128), 0, 0, 0, nullptr,
              nullptr, 0, pre_b, F, status};
-    if (f256)
+    const bool dpairs = rows >= static_cast<int64_t>(E) * 512 && d >= 1024;  // 256-row pair tiles
+    if (f256 && dpairs)
+      err = launch<DGRAD_SWIGLU, 256, true>(m_dout128, m_wd, m_wd, a,
+                                            (E + (rows + 2 * BM - 1) / (2 * BM)) * a.n_tiles, s);
+    else if (f256)
       err = launch<DGRAD_SWIGLU, 256, false>(m_dout128, m_wd, m_wd, a, mt_bound * a.n_tiles, s);
     else
       err = launch<DGRAD_SWIGLU, 128, false>(m_dout128, m_wd, m_wd, a, mt_bound * a.n_tiles, s);
