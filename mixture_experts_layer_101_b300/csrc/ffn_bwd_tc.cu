@@ -603,9 +603,11 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
 // i.e. reductions of 16 or more 64-row steps per tile: there they are limited
 // by the bytes each SM loads per MMA cycle (measured on the Mixtral-shaped
 // layer: 1.08 -> 0.87 ms and 2.12 -> 1.70 ms); with ~200 rows per expert (the
-// Switch-shaped layer) pairs lose. The SwiGLU-derivative input gradient takes
-// pairs from 512 rows per expert and a reduction over d >= 1024 (measured:
-// Switch-shaped 0.277 -> 0.258 ms, Mixtral-shaped 0.96-0.99 -> 0.92-0.94 ms).
+// Switch-shaped layer) pairs lose. The input-gradient products take pairs
+// from 512 rows per expert (256-row pair tiles): the SwiGLU-derivative one
+// when its reduction over d is >= 1024 (measured: Switch-shaped 0.277 ->
+// 0.258 ms, Mixtral-shaped 0.96-0.99 -> 0.92-0.94 ms), the gate/up one
+// (reduction over 2F) always (0.252 -> 0.231 ms and 1.49-1.52 -> 1.36 ms).
 bool use_pairs(int E, int64_t rows) { return rows >= static_cast<int64_t>(E) * 1024; }
 
 }  // namespace
@@ -678,7 +680,10 @@ moe_status launch_ffn_bwd_tc(const moe_config& c, int64_t rows, int64_t rows_pad
   {
     BwArgs a{poff, offsets, E, 2 * F / BK, F / BK, F, d / 256, 0, 0, 0, dx_perm, nullptr, d,
              nullptr, F, status};
-    err = launch<DGRAD_STORE, 256, false>(m_dpre128, m_wg, m_wu, a, mt_bound * a.n_tiles, s);
+    const bool spairs = rows >= static_cast<int64_t>(E) * 512;  // 256-row pair tiles
+    err = spairs ? launch<DGRAD_STORE, 256, true>(m_dpre128, m_wg, m_wu, a,
+                                                 (E + (rows + 2 * BM - 1) / (2 * BM)) * a.n_tiles, s)
+                 : launch<DGRAD_STORE, 256, false>(m_dpre128, m_wg, m_wu, a, mt_bound * a.n_tiles, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     trace_record(4, s);
   }
