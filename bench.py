@@ -15,7 +15,11 @@ written (L2 is 126 MB) outside the step's CUDA-event interval; the step time
 is the interval between events recorded on the launch stream by the library
 at the step's start and end. value = tokens of all ranks / max over ranks of
 the summed step time. The library's trace events also time each stage; the
-dominant kernel's roofline fraction uses that kernel's own interval.
+dominant kernel's roofline fraction uses that kernel's own interval. The
+forward step is captured once as a CUDA graph (the same kernels, the trace
+events recorded as graph nodes) and replayed each step, with a synchronise
+after each replay, outside the events, to read them; --eager launches every
+kernel per step instead.
 
 e2e: the same metric through MoELayer.forward_host: pinned host x copied in,
 the layer, y and L_aux copied out, per step, wall clock with a sync per step.
@@ -443,23 +447,42 @@ def run_ours(args, world, rank):
     torch.cuda.synchronize()
     layer.stats.status.zero_()
 
-    events = [moe.TraceEvents(nst) for _ in range(args.steps)]
+    if args.graph:
+        # the step as one CUDA graph (captured with one set of stage events,
+        # re-recorded by every replay and read after it)
+        ev = moe.TraceEvents(nst)
+        moe.moe_trace_events(ev.handles())
+        graph = layer.capture(x)
+        moe.moe_trace_events([])
+        torch.cuda.synchronize()
+        layer.stats.status.zero_()
+    else:
+        events = [moe.TraceEvents(nst) for _ in range(args.steps)]
+    step_ms, stage_ms = [], {name: [] for name in moe.TRACE_STAGES}
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler() as clocks:
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
-            moe.moe_trace_events(events[i].handles())
-            layer.forward(x)
+            if args.graph:
+                graph.replay()
+                torch.cuda.synchronize()  # outside the events: the replay's own times
+                step_ms.append(ev.elapsed_ms(0, nst - 1))
+                for j, name in enumerate(moe.TRACE_STAGES):
+                    stage_ms[name].append(ev.elapsed_ms(j, j + 1))
+            else:
+                moe.moe_trace_events(events[i].handles())
+                layer.forward(x)
         moe.moe_trace_events([])
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     barrier(world)
 
-    step_ms = [ev.elapsed_ms(0, nst - 1) for ev in events]
-    stage_ms = {name: [ev.elapsed_ms(j, j + 1) for ev in events]
-                for j, name in enumerate(moe.TRACE_STAGES)}
+    if not args.graph:
+        step_ms = [ev.elapsed_ms(0, nst - 1) for ev in events]
+        stage_ms = {name: [ev.elapsed_ms(j, j + 1) for ev in events]
+                    for j, name in enumerate(moe.TRACE_STAGES)}
     dev_s = sum(step_ms) / 1e3
     max_s = max_over_ranks(dev_s, world)
     tokens = sum_over_ranks(float(w.T * args.steps), world)
@@ -528,7 +551,8 @@ def run_ours(args, world, rank):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * max_s / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": workload_config(w, args),
+            "config": workload_config(w, args, {"launch": "cuda_graph" if args.graph else
+                                                  "stream"}),
             "roofline": roof,
             "layer_roofline": dict(layer_roof, note="whole step against max(F/peak, B/BW) "
                                                     "of the layer's algorithmic work"),
@@ -696,6 +720,9 @@ def main(argv=None):
                     help="override the workload's token count (small profiling cases)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override the workload's expert count (small profiling cases)")
+    ap.add_argument("--eager", dest="graph", action="store_false",
+                    help="forward pass: launch every kernel per step instead of replaying "
+                         "the step as one captured CUDA graph (the default)")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "train"],
                     help="forward (the layer's metric) or train: forward + backward")
     ap.add_argument("--z-coef", type=float, default=1e-3,

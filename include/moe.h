@@ -343,7 +343,9 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* w_r,
  *     [5] after its weight gradient, [6] after dx, [7] after the router
  *     weight gradient.
  * Events beyond n are not recorded. The library does not own, create or
- * destroy the events.
+ * destroy the events. On a stream that is being captured into a CUDA graph
+ * they are recorded as external event-record nodes, so every replay of the
+ * graph records them again.
  * Errors: MOE_ERR_INVALID (n outside [0, 8], or events NULL with n > 0). */
 moe_status moe_trace_events(void* const* events, int32_t n);
 

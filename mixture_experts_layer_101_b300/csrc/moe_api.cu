@@ -136,7 +136,14 @@ thread_local int g_ntrace = 0;
 }  // namespace
 
 void trace_record(int i, cudaStream_t s) {
-  if (i < g_ntrace && g_trace[i] != nullptr) cudaEventRecord(g_trace[i], s);
+  if (i >= g_ntrace || g_trace[i] == nullptr) return;
+  // inside a stream capture a plain record only orders the graph; the
+  // external form records the event each time the graph is replayed
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(g_trace[i], s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(g_trace[i], s);
 }
 
 int sm_count() {

@@ -471,6 +471,23 @@ class MoELayer:
         self._x = x
         return self.y
 
+    def capture(self, x) -> "torch.cuda.CUDAGraph":
+        """Records one forward() on the input buffer x as a CUDA graph: the
+        layer's kernels with their arguments, captured once, so that a decode
+        loop replays them (graph.replay()) without a launch per kernel. A
+        replay reads what x holds at that time and writes self.y and
+        self.stats; x, the weights and the workspace must stay where they are.
+        One eager forward runs first, so that the library's one-time
+        per-device setup (kernel attributes, the driver's tensor-map encoder)
+        stays out of the capture. Trace events registered on this thread
+        (moe_trace_events) are recorded into the graph too."""
+        self.forward(x)
+        torch.cuda.synchronize(self.ws.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.forward(x)
+        return g
+
     def backward(self, dy, z_coef: float = 0.0, grads: dict | None = None, stream=None) -> dict:
         """Gradients of <dy, y> + L_aux + z_coef * z_loss after forward() on a
         config with save_for_backward (x must be unchanged since). Returns the

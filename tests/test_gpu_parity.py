@@ -245,6 +245,32 @@ def test_full_size_workload(name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name", ["tc_pairs_both", "fused_router_switch_gate",
+                                  "simt_softmax_bias_fp32"])
+def test_graph_replay_matches_forward(name):
+    """A CUDA graph captured from forward() on a fixed input buffer, replayed
+    after new data is copied into that buffer, gives the same bits (y and
+    statistics) as an eager forward() on the new data."""
+    w = SMALL[name]
+    inp = L.device_inputs(w)
+    cfg = L.layer_config(w, inp)
+    layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
+    xbuf = inp["x"].clone()
+    graph = layer.capture(xbuf)
+    x2 = (inp["x"].float() * -0.75).to(inp["x"].dtype)  # other data, same shape
+    xbuf.copy_(x2)
+    graph.replay()
+    torch.cuda.synchronize()
+    y_graph, st_graph = layer.y.clone(), layer.stats.to_host()
+    y_eager = layer.forward(x2).clone()
+    torch.cuda.synchronize()
+    st_eager = layer.stats.to_host()
+    assert torch.equal(y_graph, y_eager)
+    for k in ("count", "kept", "f", "P"):
+        assert np.array_equal(st_graph[k], st_eager[k]), k
+    assert st_graph["l_aux"] == st_eager["l_aux"] and st_graph["status"] == 0
+
+
 def test_host_stream_matches_forward():
     """MoELayer.forward_host_stream (copies of neighbouring batches overlapped
     with compute) gives the same bits as forward() batch by batch."""
