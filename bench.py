@@ -16,10 +16,10 @@ is the interval between events recorded on the launch stream by the library
 at the step's start and end. value = tokens of all ranks / max over ranks of
 the summed step time. The library's trace events also time each stage; the
 dominant kernel's roofline fraction uses that kernel's own interval. The
-forward step is captured once as a CUDA graph (the same kernels, the trace
-events recorded as graph nodes) and replayed each step, with a synchronise
-after each replay, outside the events, to read them; --eager launches every
-kernel per step instead.
+step (forward, or forward + backward with --pass train) is captured once as
+a CUDA graph (the same kernels, the trace events recorded as graph nodes)
+and replayed each step, with a synchronise after each replay, outside the
+events, to read them; --eager launches every kernel per step instead.
 
 e2e: the same metric through MoELayer.forward_host: pinned host x copied in,
 the layer, y and L_aux copied out, per step, wall clock with a sync per step.
@@ -600,28 +600,52 @@ def run_train(args, world, rank):
         layer.forward(x)
         layer.backward(dy, z, grads)
     torch.cuda.synchronize()
+
+    def step(h):
+        moe.moe_trace_events(h[:nf])
+        layer.forward(x)
+        moe.moe_trace_events(h[nf:])
+        layer.backward(dy, z, grads)
+        moe.moe_trace_events([])
+
+    def times(ev):
+        out = {name: ev.elapsed_ms(j, j + 1) for j, name in enumerate(moe.TRACE_STAGES)}
+        out.update({name: ev.elapsed_ms(nf + j, nf + j + 1)
+                    for j, name in enumerate(moe.TRACE_STAGES_BWD)})
+        return ev.elapsed_ms(0, nf + nb - 1), out
+
+    if args.graph:  # forward + backward captured once, replayed per step
+        ev = moe.TraceEvents(nf + nb)
+        graph = moe.capture_graph(lambda: step(ev.handles()), dev)
+    else:
+        events = [moe.TraceEvents(nf + nb) for _ in range(args.steps)]
+    torch.cuda.synchronize()
     layer.stats.status.zero_()
-    events = [moe.TraceEvents(nf + nb) for _ in range(args.steps)]
+    step_ms, stage_ms = [], {n: [] for n in (*moe.TRACE_STAGES, *moe.TRACE_STAGES_BWD)}
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler() as clocks:
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
-            h = events[i].handles()
-            moe.moe_trace_events(h[:nf])
-            layer.forward(x)
-            moe.moe_trace_events(h[nf:])
-            layer.backward(dy, z, grads)
-        moe.moe_trace_events([])
+            if args.graph:
+                graph.replay()
+                torch.cuda.synchronize()  # outside the events: the replay's own times
+                t, st_i = times(ev)
+                step_ms.append(t)
+                for k, v in st_i.items():
+                    stage_ms[k].append(v)
+            else:
+                step(events[i].handles())
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     barrier(world)
-    step_ms = [ev.elapsed_ms(0, nf + nb - 1) for ev in events]
-    stage_ms = {name: [ev.elapsed_ms(j, j + 1) for ev in events]
-                for j, name in enumerate(moe.TRACE_STAGES)}
-    stage_ms.update({name: [ev.elapsed_ms(nf + j, nf + j + 1) for ev in events]
-                     for j, name in enumerate(moe.TRACE_STAGES_BWD)})
+    if not args.graph:
+        for e in events:
+            t, st_i = times(e)
+            step_ms.append(t)
+            for k, v in st_i.items():
+                stage_ms[k].append(v)
     max_s = max_over_ranks(sum(step_ms) / 1e3, world)
     value = sum_over_ranks(float(w.T * args.steps), world) / max_s
     st = layer.stats.to_host()
@@ -684,7 +708,9 @@ def run_train(args, world, rank):
             "warmup": args.warmup, "ms_per_step": round(1e3 * max_s / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
-            "config": workload_config(w, args, {"pass": "train", "z_coef": z}),
+            "config": workload_config(w, args, {"pass": "train", "z_coef": z,
+                                                  "launch": "cuda_graph" if args.graph else
+                                                  "stream"}),
             "roofline": roof,
             "step_roofline": dict(step_roof, note="whole training step against "
                                                   "max(F/peak, B/BW) of its algorithmic work"),
@@ -721,8 +747,8 @@ def main(argv=None):
     ap.add_argument("--experts", type=int, default=None,
                     help="override the workload's expert count (small profiling cases)")
     ap.add_argument("--eager", dest="graph", action="store_false",
-                    help="forward pass: launch every kernel per step instead of replaying "
-                         "the step as one captured CUDA graph (the default)")
+                    help="launch every kernel per step instead of replaying the step as one "
+                         "captured CUDA graph (the default)")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "train"],
                     help="forward (the layer's metric) or train: forward + backward")
     ap.add_argument("--z-coef", type=float, default=1e-3,

@@ -7,17 +7,17 @@ this package is its ctypes binding. Build the library with
 """
 from .moe import (EXPORTED, GRAD_NAMES, LIB_PATH, TRACE_STAGES, TRACE_STAGES_BWD, LayerConfig,
                   MoEError, MoELayer, Stats, TraceEvents, a_max, alloc_grads, alloc_workspace,
-                  backward_launch_count, capacity, ffn_uses_tensor_cores, forward_launch_count,
-                  load_library, moe_backward, moe_backward_launch_count, moe_combine,
-                  moe_dispatch, moe_expert_ffn, moe_forward, moe_route, moe_route_no_workspace,
-                  moe_selftest_bounded_wait, moe_status_string, moe_trace_events,
-                  moe_workspace_size, rows_max, status_string, workspace_size)
+                  backward_launch_count, capacity, capture_graph, ffn_uses_tensor_cores,
+                  forward_launch_count, load_library, moe_backward, moe_backward_launch_count,
+                  moe_combine, moe_dispatch, moe_expert_ffn, moe_forward, moe_route,
+                  moe_route_no_workspace, moe_selftest_bounded_wait, moe_status_string,
+                  moe_trace_events, moe_workspace_size, rows_max, status_string, workspace_size)
 
 __all__ = ["EXPORTED", "GRAD_NAMES", "LIB_PATH", "TRACE_STAGES", "TRACE_STAGES_BWD",
            "LayerConfig", "MoEError", "MoELayer", "Stats", "TraceEvents", "a_max", "alloc_grads",
-           "alloc_workspace", "backward_launch_count", "capacity", "ffn_uses_tensor_cores",
-           "forward_launch_count", "load_library", "moe_backward", "moe_backward_launch_count",
-           "moe_combine", "moe_dispatch", "moe_expert_ffn", "moe_forward", "moe_route",
-           "moe_route_no_workspace", "moe_selftest_bounded_wait", "moe_status_string",
-           "moe_trace_events", "moe_workspace_size", "rows_max", "status_string",
-           "workspace_size"]
+           "alloc_workspace", "backward_launch_count", "capacity", "capture_graph",
+           "ffn_uses_tensor_cores", "forward_launch_count", "load_library", "moe_backward",
+           "moe_backward_launch_count", "moe_combine", "moe_dispatch", "moe_expert_ffn",
+           "moe_forward", "moe_route", "moe_route_no_workspace", "moe_selftest_bounded_wait",
+           "moe_status_string", "moe_trace_events", "moe_workspace_size", "rows_max",
+           "status_string", "workspace_size"]

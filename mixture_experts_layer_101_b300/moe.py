@@ -452,6 +452,21 @@ TRACE_STAGES_BWD = ["bwd_combine_router", "bwd_down_dgrad", "bwd_down_wgrad",
                     "bwd_gate_up_dgrad", "bwd_gate_up_wgrad", "bwd_dx", "bwd_router_wgrad"]
 
 
+def capture_graph(fn, device=None) -> "torch.cuda.CUDAGraph":
+    """Runs fn() (a sequence of library calls on the current stream) once
+    eagerly, so that the library's one-time per-device setup (kernel
+    attributes, the driver's tensor-map encoder) stays out of the capture,
+    then records fn() as a CUDA graph; graph.replay() runs the same kernels
+    with the same arguments again. Trace events registered while fn runs
+    (moe_trace_events) are recorded into the graph too."""
+    fn()
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
 class MoELayer:
     """A sparse-MoE FFN layer with its weights, workspace and statistics held
     on one CUDA device; forward() runs moe_forward."""
@@ -476,17 +491,9 @@ class MoELayer:
         layer's kernels with their arguments, captured once, so that a decode
         loop replays them (graph.replay()) without a launch per kernel. A
         replay reads what x holds at that time and writes self.y and
-        self.stats; x, the weights and the workspace must stay where they are.
-        One eager forward runs first, so that the library's one-time
-        per-device setup (kernel attributes, the driver's tensor-map encoder)
-        stays out of the capture. Trace events registered on this thread
-        (moe_trace_events) are recorded into the graph too."""
-        self.forward(x)
-        torch.cuda.synchronize(self.ws.device)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            self.forward(x)
-        return g
+        self.stats; x, the weights and the workspace must stay where they
+        are."""
+        return capture_graph(lambda: self.forward(x), self.ws.device)
 
     def backward(self, dy, z_coef: float = 0.0, grads: dict | None = None, stream=None) -> dict:
         """Gradients of <dy, y> + L_aux + z_coef * z_loss after forward() on a

@@ -121,6 +121,40 @@ def test_backward_deterministic():
             assert torch.equal(v, g2[k]), k
 
 
+@pytest.mark.parametrize("name", ["bf16_capacity_residual_z", "bf16_pair_tails_mixed"])
+def test_training_step_graph_replay(name):
+    """forward + backward captured as one CUDA graph and replayed after new x
+    and dy are copied into their buffers gives the same bits as the eager
+    calls on the new data."""
+    w, z = CASES[name]
+    cfg, inp, dy = inputs(w)
+    cfg.save_for_backward = True
+    layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
+    xbuf, dybuf = inp["x"].clone(), dy.clone()
+    grads = moe.alloc_grads(cfg, inp["b_r"] is not None)
+
+    def step():
+        layer.forward(xbuf)
+        layer.backward(dybuf, z, grads)
+
+    graph = moe.capture_graph(step)
+    x2 = (inp["x"].float() * -0.75).to(inp["x"].dtype)
+    dy2 = (dy.float() * 1.5).to(dy.dtype)
+    xbuf.copy_(x2)
+    dybuf.copy_(dy2)
+    graph.replay()
+    torch.cuda.synchronize()
+    g_graph = {k: v.clone() for k, v in grads.items() if v is not None}
+    y_graph = layer.y.clone()
+    layer.forward(x2)
+    layer.backward(dy2, z, grads)
+    torch.cuda.synchronize()
+    assert torch.equal(y_graph, layer.y)
+    for k, v in g_graph.items():
+        assert torch.equal(v, grads[k]), k
+    assert layer.stats.to_host()["status"] == 0
+
+
 def test_backward_needs_saved_state():
     w, _ = CASES["bf16_top2"]
     cfg, inp, dy = inputs(w)
