@@ -47,8 +47,8 @@ SMALL = {
     # CTA pairs (several tiles per expert and a reduction of >= 1024): both
     # GEMMs in pairs
     "tc_pairs_both": wl(T=1500, d=2048, F=2048, N=2, K=2),
-    "tc_pairs_down_only": wl(T=2048, d=1024, F=2048, N=2, K=1, n_shared=1,
-                             capacity_factor=1.5, add_residual=True),
+    "tc_pairs_shared_capacity": wl(T=2048, d=1024, F=2048, N=2, K=1, n_shared=1,
+                                   capacity_factor=1.5, add_residual=True),
     # CTA pairs with expert tails on both sides of 128 rows (a last pair tile
     # whose odd CTA holds no rows, or some) and exact multiples of 256 under a
     # capacity (expert counts 1012 1009 1027 1048; the same capped at 1024;
@@ -70,7 +70,7 @@ SMALL = {
     "tc_shared_one": wl(T=300, d=256, F=256, N=8, K=2, n_shared=1),
     "tc_shared_two_capacity": wl(T=600, d=512, F=128, N=16, K=2, n_shared=2,
                                  capacity_factor=0.5, add_residual=True),
-    "tc_shared_pairs": wl(T=2048, d=256, F=256, N=2, K=1, n_shared=1),
+    "tc_shared_many_tiles": wl(T=2048, d=256, F=256, N=2, K=1, n_shared=1),
     "simt_shared_gelu_fp32": wl(T=90, d=64, F=96, N=4, K=2, n_shared=2, dtype="f32",
                                 activation="gelu", has_bias=True, init="uniform"),
     # router selection fused into the tensor-core router's epilogue (one K
