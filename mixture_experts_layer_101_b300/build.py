@@ -4,7 +4,7 @@
 
 Each csrc/*.cu file is compiled to an object in parallel, then linked into
 mixture_experts_layer_101_b300/_lib/libmoe.so (the CUDA runtime is linked
-statically; the driver's tensor-map encoder is looked up at run time, so
+statically; the CUDA driver's tensor-map encoder is looked up at run time, so
 there is no link-time dependency on libcuda).
 """
 from __future__ import annotations

@@ -455,7 +455,7 @@ TRACE_STAGES_BWD = ["bwd_combine_router", "bwd_down_dgrad", "bwd_down_wgrad",
 def capture_graph(fn, device=None) -> "torch.cuda.CUDAGraph":
     """Runs fn() (a sequence of library calls on the current stream) once
     eagerly, so that the library's one-time per-device setup (kernel
-    attributes, the driver's tensor-map encoder) stays out of the capture,
+    attributes, the CUDA driver's tensor-map encoder) stays out of the capture,
     then records fn() as a CUDA graph; graph.replay() runs the same kernels
     with the same arguments again. Trace events registered while fn runs
     (moe_trace_events) are recorded into the graph too."""
