@@ -1,0 +1,68 @@
+"""Host-side arithmetic of bench.py (no GPU): the algorithmic FLOPs and bytes
+that the roofline fractions divide by, checked against the layer's shapes
+worked out by hand, and the roofline entry's choice of bound."""
+import math
+
+import pytest
+
+import bench
+import moe_inputs
+
+
+def test_prefill_gate_up_and_down_work():
+    # Mixtral-shaped prefill: 8192 kept assignments, all 8 experts active
+    w = moe_inputs.WORKLOADS["mixtral_prefill"]
+    work = bench.algorithmic_work(w, 8192, 8)
+    gu_f, gu_b = work["gate_up"]
+    dn_f, dn_b = work["down"]
+    assert gu_f == 2 * 8192 * 4096 * (2 * 14336)                   # 1.924 TFLOP
+    assert gu_b == 8 * 2 * 14336 * 4096 * 2 + 8192 * 4096 * 2 + 8192 * 14336 * 2
+    assert gu_b == 2181038080
+    assert dn_f == 2 * 8192 * 14336 * 4096
+    assert dn_b == 8 * 14336 * 4096 * 2 + 8192 * 14336 * 2 + 8192 * 4096 * 4
+    lf, lb = work["layer"]
+    assert lf == gu_f + dn_f == 6 * 8192 * 4096 * 14336
+    # every active expert's three matrices once, x in, y out, the fp32 router
+    assert lb == 8 * 3 * 14336 * 4096 * 2 + 2 * 4096 * 4096 * 2 + 8 * 4096 * 4
+
+
+def test_inactive_experts_cost_no_weight_bytes():
+    w = moe_inputs.WORKLOADS["switch_skewed"]
+    a = bench.algorithmic_work(w, 12316, 64)["gate_up"][1]
+    b = bench.algorithmic_work(w, 12316, 32)["gate_up"][1]
+    assert a - b == 32 * 2 * w.F * w.d * 2
+
+
+def test_backward_work_is_twice_the_forward_flops():
+    w = moe_inputs.WORKLOADS["mixtral_prefill"]
+    bw = bench.backward_work(w, 8192, 8)
+    fw = bench.algorithmic_work(w, 8192, 8)
+    bwd_flops = sum(bw[k][0] for k in ("bwd_down_dgrad", "bwd_down_wgrad",
+                                        "bwd_gate_up_dgrad", "bwd_gate_up_wgrad"))
+    assert bwd_flops == 2 * fw["layer"][0]
+    assert bw["step"][0] == 3 * fw["layer"][0]
+    # the weight-gradient launches write every expert's fp32 gradients
+    E, d, F = w.N, w.d, w.F
+    assert bw["bwd_gate_up_wgrad"][1] >= E * 2 * F * d * 4
+    assert bw["bwd_down_wgrad"][1] >= E * d * F * 4
+
+
+PEAKS = {"hbm_gbs": 6500.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def test_roofline_picks_the_larger_roofline_time():
+    # 1.8 TFLOP and 1 GB: 1 ms on the tensor cores, 0.15 ms of HBM -> tensor
+    r = bench.roofline_entry(1.8e12, 1e9, 2e-3, PEAKS)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert math.isclose(r["achieved"], 900.0) and math.isclose(r["frac"], 0.5)
+    # 1 GFLOP and 6.5 GB: HBM-bound
+    r = bench.roofline_entry(1e9, 6.5e9, 2e-3, PEAKS)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert math.isclose(r["achieved"], 3250.0) and math.isclose(r["frac"], 0.5)
+
+
+def test_roofline_sustained_peak_when_power_capped():
+    r = bench.roofline_entry(1.4e12, 1e9, 1e-3, PEAKS, sustained=True)
+    assert r["peak"] == 1400.0 and math.isclose(r["frac"], 1.0)
+    r = bench.roofline_entry(1.4e12, 1e9, 1e-3, PEAKS, sustained=False)
+    assert r["peak"] == 1800.0 and r["frac"] == pytest.approx(1400 / 1800, abs=1e-4)
