@@ -1,6 +1,7 @@
-"""Host-side arithmetic of bench.py (no GPU): the algorithmic FLOPs and bytes
-that the roofline fractions divide by, checked against the layer's shapes
-worked out by hand, and the roofline entry's choice of bound."""
+"""Host-side logic of bench.py (no GPU): the algorithmic FLOPs and bytes that
+the roofline fractions divide by, checked against the layer's shapes worked
+out by hand; the roofline entry's choice of bound and peak; the clock
+summary's decoding of NVML clock-event reasons (with a fake reader)."""
 import math
 
 import pytest
@@ -66,3 +67,42 @@ def test_roofline_sustained_peak_when_power_capped():
     assert r["peak"] == 1400.0 and math.isclose(r["frac"], 1.0)
     r = bench.roofline_entry(1.4e12, 1e9, 1e-3, PEAKS, sustained=False)
     assert r["peak"] == 1800.0 and r["frac"] == pytest.approx(1400 / 1800, abs=1e-4)
+
+
+class _FakeNvml:
+    """Stands in for the NVML reader: a clock trace and reason bits."""
+
+    def __init__(self):
+        self.mhz = iter([2032, 1995, 1260, 1250, 1255] + [1255] * 1000)
+        self.bits = iter([0x1, 0x4, 0x4 | 0x8] + [0x4] * 1000)
+
+    def sm_max_mhz(self):
+        return 2032
+
+    def sm_mhz(self):
+        return next(self.mhz)
+
+    def reasons(self):
+        return next(self.bits)
+
+
+def test_clock_summary_decodes_reasons(monkeypatch):
+    monkeypatch.setattr(bench, "_NvmlReader", _FakeNvml)
+    cs = bench.ClockSampler(period_s=0.0)
+    for _ in range(5):  # the sampling thread's work, done inline
+        cs.samples.append(cs.nvml.sm_mhz())
+        cs.reason_bits |= cs.nvml.reasons()
+    s = cs.summary()
+    assert s["sm_max_mhz"] == 2032 and s["samples"] == 5
+    assert s["sm_mhz"] == 1260                       # median of the five samples
+    assert s["reasons"] == ["sw_power_cap", "hw_slowdown"]   # gpu_idle is not reported
+
+
+def test_clock_summary_without_nvml(monkeypatch):
+    def broken():
+        raise RuntimeError("no device")
+    monkeypatch.setattr(bench, "_NvmlReader", broken)
+    with bench.ClockSampler() as cs:
+        pass
+    s = cs.summary()
+    assert s["sm_mhz"] is None and s["reasons"] == [] and "nvml unavailable" in s["note"]
