@@ -1,6 +1,6 @@
 /*
- * moe.h — C ABI of libmoe: the forward pass of a sparse Mixture-of-Experts
- * FFN layer on one NVIDIA B300 (sm_103a).
+ * moe.h — C ABI of libmoe: the forward and backward passes of a sparse
+ * Mixture-of-Experts FFN layer on one NVIDIA B300 (sm_103a).
  *
  * Sources (web pages on Mixture-of-Experts layers; cited by title + section):
  *   [MoE核心思想]  "MoE 的核心思想" (wmrh.cn/news/98181): 公式表达重点,
@@ -30,7 +30,10 @@
  *    aligned; its contents on entry are ignored.
  *  - Asynchrony: every call only enqueues kernels on `stream` (0 = legacy
  *    default stream) and returns. Results are valid after the stream is
- *    synchronised.
+ *    synchronised. No call synchronises or allocates, so after one call on
+ *    a device (which sets kernel attributes and looks up the CUDA driver's
+ *    tensor-map encoder) the calls can be captured into a CUDA graph and
+ *    replayed with the same buffers.
  *  - Errors: every argument error that the host can see (NULL pointer,
  *    misalignment, bad sizes, unsupported combination) is returned before
  *    anything is launched. Errors found on the device (a bounded wait that
