@@ -106,3 +106,27 @@ def test_clock_summary_without_nvml(monkeypatch):
         pass
     s = cs.summary()
     assert s["sm_mhz"] is None and s["reasons"] == [] and "nvml unavailable" in s["note"]
+
+
+def test_reference_arm_json_line():
+    """bench.py --impl reference (the float64 oracle on the host) prints one
+    JSON line with the contract's keys; it needs no GPU."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "mixtral_decode", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["value"] > 0 and j["unit"] == "tokens/s"
+    assert j["steps"] == 1 and j["warmup"] == 1 and j["higher_is_better"] is True
+    assert j["config"]["workload"] == "mixtral_decode"
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["cpu_baseline"]["value"] == j["value"]
+    assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
