@@ -9,11 +9,19 @@ Comparison rules:
     compared against the oracle re-run on the GPU's routing;
   * counts, kept, offsets, slots, token order and the drop set: bit-exact;
   * gates: |err| <= 1e-5; P and L_aux: relative error <= 1e-5;
-  * y: max |err| <= 1e-4 * rms(y) for fp32 layers, <= 2e-2 * rms(y) for bf16
-    (the bars of the named workloads); for the small and random bf16 layers,
-    where K=1 or small outputs leave nothing to average the bf16 roundings of
-    h and y, each element must lie within the bound those roundings allow
-    (bf16_rounding_bound).
+  * y, fp32 layers: max |err| <= 1e-4 * rms(y);
+  * y, bf16 layers, three checks:
+      - the stated bar on the value y is rounded from: every y_gpu element is
+        the bf16 rounding of some value within 2e-2 * rms(y) of the exact y,
+        i.e. y lies within 2e-2 * rms(y) of the interval of reals that round
+        to y_gpu (stored_bar_excess); the bf16 storage of y alone can be off
+        by 2^-8 |y|, which at the largest |y| of a 16-million-element output
+        (about 5.5 rms) is already 0.021 rms;
+      - the per-element bound of the bf16 roundings the path performs
+        (bf16_rounding_bound: h and y rounded once each);
+      - the raw bar max |err| <= 2e-2 * rms(y) (strict=True), for the layers
+        whose outputs meet it; the others are listed with their measured
+        ratios where they are tested.
 """
 from __future__ import annotations
 
@@ -41,6 +49,37 @@ def stored_cf(cfg) -> float:
 
 def y_tolerance(dtype: str) -> float:
     return 1e-4 if dtype == "f32" else 2e-2
+
+
+def bf16_neighbours(v: torch.Tensor):
+    """The bf16 values just below and just above each element of the bf16
+    tensor v (as float64 numpy arrays), by stepping its bit pattern; zero's
+    neighbours are the smallest subnormals."""
+    bits = v.contiguous().view(torch.int16).to(torch.int32)
+    neg = bits < 0
+    mag = bits & 0x7FFF
+    up_mag = torch.where(neg, mag - 1, mag + 1)      # towards +inf
+    dn_mag = torch.where(neg, mag + 1, mag - 1)      # towards -inf
+    # zero (either sign): the neighbours are +-smallest subnormal
+    zero = mag == 0
+    up_bits = torch.where(zero, torch.ones_like(bits), torch.where(neg, up_mag | 0x8000, up_mag))
+    dn_bits = torch.where(zero, torch.full_like(bits, 0x8001),
+                          torch.where(neg, dn_mag | 0x8000, dn_mag))
+    as_bf16 = lambda b: (b & 0xFFFF).to(torch.int16).view(torch.bfloat16).double().numpy()
+    return as_bf16(dn_bits), as_bf16(up_bits)
+
+
+def stored_bar_excess(y_gpu: torch.Tensor, y_ref: np.ndarray, tol: float) -> float:
+    """max over elements of the distance (beyond tol) from the exact y to the
+    interval of reals that round to y_gpu in bf16 (round to nearest: half the
+    gap to each neighbour). <= 0 means every y_gpu element is the rounding of
+    some value within tol of y."""
+    v = y_gpu.double().numpy()
+    dn, up = bf16_neighbours(y_gpu)
+    lo = v - (v - dn) / 2.0
+    hi = v + (up - v) / 2.0
+    dist = np.maximum(lo - y_ref, y_ref - hi)
+    return float(np.max(dist - tol, initial=-np.inf))
 
 
 def device_inputs(w: moe_inputs.MoEWorkload):
@@ -150,10 +189,14 @@ def bf16_rounding_bound(cfg: moe.LayerConfig, inp: dict, ref: dict) -> np.ndarra
 
 
 def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
-                bound: str = "rms"):
+                strict: bool = True, stored: bool = True):
     """Compare a stage-wise GPU run against the oracle. tokens: the tokens
     whose y is checked (None = all); routing, statistics and dispatch always
-    cover every token. Returns a summary dict."""
+    cover every token. bf16 layers always meet the per-element rounding
+    bound; strict: also max |err| <= 2e-2 * rms(y) on the raw output; stored:
+    also the 2e-2 * rms(y) bar on the value y is rounded from (see the module
+    notes). Returns a summary dict (near-tie tokens, tokens whose routing
+    differs from the oracle's, max |err| / rms(y), ...)."""
     K, N = cfg.top_k, cfg.n_experts
     x, w_r, b_r = inp["x"].cpu(), inp["w_r"].cpu(), None if inp["b_r"] is None else inp["b_r"].cpu()
     sb = None if cfg.select_bias is None else cfg.select_bias.cpu()
@@ -199,12 +242,18 @@ def check_layer(cfg: moe.LayerConfig, inp: dict, gpu: dict, *, tokens=None,
     y_ref = ref["y"]
     rms = float(np.sqrt(np.mean(y_ref ** 2))) if y_ref.size else 0.0
     err = float(np.max(np.abs(y_gpu - y_ref))) if y_ref.size else 0.0
-    if bound == "rounding" and cfg.dtype == "bf16":
+    tol = y_tolerance(cfg.dtype) * rms
+    if cfg.dtype == "bf16":
+        # the stated bar on the value the stored y was rounded from
+        if stored:
+            excess_stored = stored_bar_excess(gpu["y"][torch.as_tensor(tok)], y_ref, tol)
+            assert excess_stored <= 0.0, ("stored bar", err, rms, excess_stored)
         # per-element bound from the bf16 roundings the path performs
         excess = np.abs(y_gpu - y_ref) - bf16_rounding_bound(cfg, inp, ref)
-        assert excess.max(initial=-1.0) <= 0.0, (err, rms, float(excess.max()))
-    else:
-        assert err <= y_tolerance(cfg.dtype) * rms + 1e-30, (err, rms)
+        assert excess.max(initial=-1.0) <= 0.0, ("rounding bound", err, rms,
+                                                 float(excess.max()))
+    if cfg.dtype != "bf16" or strict:
+        assert err <= tol + 1e-30, ("raw bar", err, rms, err / rms if rms > 0 else 0.0)
     return {"near_ties": n_near, "routing_diff": n_diff, "A": A, "y_err_over_rms":
             err / rms if rms > 0 else 0.0, "n_dropped": ref["n_dropped"]}
 

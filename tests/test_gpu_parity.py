@@ -1,10 +1,9 @@
 """GPU parity: the CUDA path, called through the C ABI, against the float64
 oracle on the same seeded inputs.
 
-Small shapes (every token checked) span several tiles with ragged tails and
-cover both expert-FFN paths (tcgen05 tensor cores and CUDA cores); the five
-named workloads run at full size with routing, statistics and dispatch
-checked on every token and y on a sample of tokens.
+Small shapes span several tiles with ragged tails and cover both expert-FFN
+paths (tcgen05 tensor cores and CUDA cores); the named workloads run at full
+size. Every token is checked everywhere: routing, statistics, dispatch and y.
 """
 import math
 
@@ -49,6 +48,9 @@ SMALL = {
     "tc_pairs_both": wl(T=1500, d=2048, F=2048, N=2, K=2),
     "tc_pairs_shared_capacity": wl(T=2048, d=1024, F=2048, N=2, K=1, n_shared=1,
                                    capacity_factor=1.5, add_residual=True),
+    # K = 1, pairs: the down projection's pair epilogue writes y (combine fused)
+    "tc_pairs_top1_capacity": wl(T=2048, d=1024, F=2048, N=2, K=1, capacity_factor=0.9,
+                                 add_residual=True, router_bias="uniform"),
     # CTA pairs with expert tails on both sides of 128 rows (a last pair tile
     # whose odd CTA holds no rows, or some) and exact multiples of 256 under a
     # capacity (expert counts 1012 1009 1027 1048; the same capped at 1024;
@@ -64,6 +66,9 @@ SMALL = {
     "tc_select_bias": wl(T=500, d=256, F=128, N=16, K=4, select_bias="uniform"),
     "tc_switch_gate_capacity": wl(T=1000, d=256, F=128, N=8, K=1, gate_mode="softmax",
                                   capacity_factor=1.25, add_residual=True),
+    # K = 1 without the residual: dropped tokens come out as zeros
+    "tc_top1_drops_no_residual": wl(T=1000, d=512, F=256, N=8, K=1, capacity_factor=0.5,
+                                    router_bias="skew"),
     "simt_softmax_bias_fp32": wl(T=100, d=36, F=52, N=6, K=3, dtype="f32", init="uniform",
                                  gate_mode="softmax", select_bias="uniform"),
     # shared experts: every token, gate 1, outside capacity
@@ -97,17 +102,45 @@ SMALL = {
 }
 
 
+# bf16 shapes whose raw max |err| / rms(y) exceeds the stated 2e-2 (measured
+# ratios on B300; every other bf16 shape above meets it): few output columns
+# or K = 1 leave nothing to average the bf16 roundings of h and y over, and
+# the largest |y| of a large output sits in a binade whose half-ulp alone is
+# near 2e-2 rms. They meet the stated bar on the value y is rounded from and
+# the per-element rounding bound (see moe_testlib).
+RAW_BAR_EXCEPTIONS = {
+    "fused_router_chunks": 0.0270,     # T=19500, F=64: 5 M outputs, 64-term h sums
+    "tc_shared_many_tiles": 0.0241,    # K=1 + one shared expert, gate 1 on both
+    "tc_pair_tails_k3": 0.0206,
+    # no residual and half the assignments dropped: y is exactly 0 on the
+    # dropped tokens, so rms(y) over all tokens is 0.7 of the computed
+    # outputs' rms (0.025 of theirs); neither 2e-2 bar is met, the
+    # per-element rounding bound is
+    "tc_top1_drops_no_residual": 0.0355,
+}
+STORED_BAR_EXCEPTIONS = {"tc_top1_drops_no_residual"}
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_layers_stagewise(name):
     w = SMALL[name]
     inp = L.device_inputs(w)
     cfg = L.layer_config(w, inp)
     gpu = L.run_stages(cfg, inp)
-    summary = L.check_layer(cfg, inp, gpu, bound="rounding")
+    summary = L.check_layer(cfg, inp, gpu, strict=name not in RAW_BAR_EXCEPTIONS,
+                            stored=name not in STORED_BAR_EXCEPTIONS)
     assert summary["routing_diff"] == 0 or summary["near_ties"] > 0
+    print(f"PARITY {name} {summary}")
 
 
-@pytest.mark.parametrize("name", ["tc_ragged", "tiny_fp32", "tc_top1_capacity"])
+# moe_forward fuses the combine into the down projection when K = 1 and there
+# are no shared experts (tc_top1_*, tc_single_expert, tc_switch_gate_capacity,
+# tc_pairs_shared_capacity has a shared expert and does not): it must give
+# the stage-wise path's bits.
+@pytest.mark.parametrize("name", ["tc_ragged", "tiny_fp32", "tc_top1_capacity",
+                                  "tc_top1_drops_no_residual", "tc_single_expert",
+                                  "tc_switch_gate_capacity", "tc_pairs_shared_capacity",
+                                  "tc_many_tiles_capacity", "tc_pairs_top1_capacity"])
 def test_forward_equals_stages_and_is_deterministic(name):
     w = SMALL[name]
     cfg = moe.LayerConfig.from_workload(w)
@@ -218,8 +251,13 @@ def test_host_errors_launch_nothing():
 
 
 # ------------------------------------------------ the named workloads ----
-FULL_SAMPLE = {"mixtral_prefill": 24, "mixtral_decode": 16, "deepseek_fine": 8,
-               "deepseek_shared": 8, "switch_skewed": 48}
+# y is checked on every token of every named workload. Raw max |err| / rms(y)
+# measured on B300 (the stated 2e-2 bar is asserted on the raw output where it
+# holds; prefill and the DeepSeek-shaped layers exceed it by the bf16 storage
+# of y at their largest |y|, and meet it on the value y is rounded from):
+#   mixtral_decode 0.0130, switch_skewed 0.0162, mixtral_prefill 0.0207,
+#   deepseek_fine 0.0289, deepseek_shared 0.0197.
+FULL_RAW_BAR = {"mixtral_decode", "switch_skewed", "deepseek_shared"}
 
 
 @pytest.mark.parametrize("name", ["mixtral_decode", "switch_skewed", "mixtral_prefill",
@@ -229,18 +267,15 @@ def test_full_size_workload(name):
     cfg = moe.LayerConfig.from_workload(w)
     inp = L.device_inputs(w)
     gpu = L.run_stages(cfg, inp)
-    rng = np.random.default_rng(12345)
-    n = min(FULL_SAMPLE[name], w.T)
-    tokens = np.sort(rng.choice(w.T, size=n, replace=False))
-    if name == "switch_skewed":  # include dropped tokens: their y must equal x
-        dropped = np.nonzero((gpu["slot_of"].numpy() < 0).all(axis=1))[0]
-        tokens = np.union1d(tokens, dropped[:8])
-    summary = L.check_layer(cfg, inp, gpu, tokens=tokens)
+    summary = L.check_layer(cfg, inp, gpu, tokens=None, strict=name in FULL_RAW_BAR)
+    print(f"PARITY {name} {summary}")
     y_fwd, _ = L.run_forward(cfg, inp)
     assert torch.equal(y_fwd, gpu["y"])
     if name == "switch_skewed":
         assert moe.capacity(cfg) == 640
         assert summary["n_dropped"] > 0
+        dropped = (gpu["slot_of"].numpy() < 0).all(axis=1)
+        assert torch.equal(gpu["y"][torch.as_tensor(dropped)], inp["x"].cpu()[dropped])
     del inp
     torch.cuda.empty_cache()
 
@@ -348,6 +383,6 @@ def test_random_layers(w):
     inp = L.device_inputs(w)
     cfg = L.layer_config(w, inp)
     gpu = L.run_stages(cfg, inp)
-    L.check_layer(cfg, inp, gpu, bound="rounding")
+    L.check_layer(cfg, inp, gpu, strict=False)
     y_fwd, _ = L.run_forward(cfg, inp)
     assert torch.equal(y_fwd, gpu["y"])
