@@ -194,16 +194,23 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r,
  * no counterpart: this is an interface variant, not a different method).
  * A serving process whose device memory is all owned by its own pool, or a
  * plug-in interface that passes no workspace, can call this instead of
- * moe_route: same kernels, same results, but the per-block partial sums of
- * the statistics live in a fixed array inside the library (1 MiB, held on
- * every GPU that loads the library until the process exits) instead of a
- * caller workspace. Nothing is allocated: no cudaMalloc, no cudaFree.
+ * moe_route. It always runs the CUDA-core (FFMA) router and the statistics
+ * kernels of moe_route, with the per-block partial sums of the statistics in
+ * a fixed array inside the library (1 MiB, held on every GPU that loads the
+ * library until the process exits) instead of a caller workspace. Nothing is
+ * allocated: no cudaMalloc, no cudaFree.
+ *   Results: those of moe_route, except that for bf16 layers with
+ *   d % 64 == 0 moe_route takes the tensor-core router, which sums the logits
+ *   in another order: the choice can then differ on near-tie tokens (some
+ *   adjacent gap among the K+1 largest logits below 1e-5), and this call can
+ *   be slower on those layers.
  *   Limit: ceil(T / 32) * (N + 2) <= 131072 (e.g. T <= 16256 with N = 256,
  *   T <= 419424 with N = 8); beyond it returns MOE_ERR_WORKSPACE before
  *   launching anything.
- *   Set-up: the first call on each device looks up the array's device
- *   address (cudaGetSymbolAddress) with that device current; make that first
- *   call before any stream capture on that device.
+ *   Set-up: the first call in each CUDA context (normally once per device:
+ *   the runtime's primary context) looks up the array's device address
+ *   (cudaGetSymbolAddress) with that context current; make that first call
+ *   before any stream capture on that device.
  *   Sharing: all calls share the array and it keeps the last call's
  *   contents; each call rewrites every element it reads, so nothing needs
  *   clearing, but calls whose kernels overlap on the GPU (other streams or
@@ -331,6 +338,77 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* w_r,
                         const moe_expert_weights* weights, const void* dy,
                         float z_coef, moe_grads* grads, moe_stats* stats,
                         void* ws, moe_stream_t stream);
+
+/* ---- Expert-parallel staging ------------------------------------------
+ * The local data movement around the two all-to-alls of an expert-parallel
+ * layer ("MoE 的核心思想", Expert Parallelism and 前向传播中的 All-to-All 通信:
+ * the experts are spread over R devices; in the dispatch step every device
+ * sends its tokens to the devices that hold their experts, each device runs
+ * its own experts on what it received, and in the combine step the outputs
+ * return to their source devices for the gate-weighted sum). These calls
+ * only lay rows out on one device; the caller exchanges the buffers with its
+ * own collective (e.g. an all-to-all with the split sizes below).
+ * Placement: owner[e] in [0, R) is the device that holds expert e (DEVICE
+ * [N] int32); the pages name no placement. Capacity and dispatch stay per
+ * source device (moe_dispatch on its own tokens). Shared experts are not
+ * exchanged: these calls need cfg->n_shared == 0 (MOE_ERR_UNSUPPORTED).
+ * Every call is two launches on `stream`: a one-block plan kernel that writes
+ * position tables into ws (>= moe_ep_workspace_size bytes, 256-byte aligned;
+ * contents on entry ignored) and a row-copy kernel. Rows move bit for bit.
+ * Device-detected errors go to stats->status (stats may be NULL) and then
+ * no row is written: MOE_ERR_INDEX for an owner outside [0, R), a negative
+ * count or offsets that no dispatch writes; MOE_ERR_WORKSPACE when a
+ * device would receive more than rows_cap rows. Limits: 1 <= R <= 256. */
+
+/* Bytes of workspace the four calls below need for cfg and R devices
+ * (about 8 * N * R bytes); 0 if cfg or n_ranks is invalid. */
+size_t moe_ep_workspace_size(const moe_config* cfg, int32_t n_ranks);
+
+/* Dispatch step, source device: x_perm [A_max][d] (cfg->dtype, expert e at
+ * rows [offsets[e], offsets[e+1]) as moe_dispatch writes them) laid out by
+ * destination into send [A_max][d]: destination r ascending, then r's
+ * experts ascending, then each expert's rows in slot order.
+ * send_counts [R] int32 (DEVICE, out): rows for each destination (their
+ * exclusive prefix sums are the send offsets). The rows sent to r hold
+ * kept[e] rows for each of r's experts e ascending, so a receiver knows its
+ * layout from every source's kept[N] (gathered into kept_all below). */
+moe_status moe_ep_pack(const moe_config* cfg, int32_t n_ranks, const int32_t* owner,
+                       const int32_t* offsets, const void* x_perm, void* send,
+                       int32_t* send_counts, moe_stats* stats, void* ws,
+                       moe_stream_t stream);
+
+/* Local-compute set-up on device `rank`: recv (rows from every source s
+ * ascending, each source's rows for this device in the order it sent them)
+ * rearranged into x_local, expert-major: this device's experts ascending
+ * (local index j), then sources ascending. kept_all [R][N] int32 (DEVICE):
+ * kept[e] of every source s. local_offsets [N+1] int32 (DEVICE, out):
+ * local expert j's rows are [local_offsets[j], local_offsets[j+1]) for j <
+ * E_r (the number of experts with owner == rank); entries E_r..N hold the
+ * total. recv and x_local hold rows_cap rows of d elements (cfg->dtype).
+ * The experts then run with moe_expert_ffn on a config with n_experts = E_r,
+ * top_k = 1, no capacity and T >= the total rows, the offsets
+ * local_offsets and the weights of this device's experts stacked in
+ * ascending expert order. */
+moe_status moe_ep_regroup(const moe_config* cfg, int32_t n_ranks, int32_t rank,
+                          const int32_t* owner, const int32_t* kept_all, int64_t rows_cap,
+                          const void* recv, void* x_local, int32_t* local_offsets,
+                          moe_stats* stats, void* ws, moe_stream_t stream);
+
+/* The inverse of moe_ep_regroup on the expert outputs: o_local [rows_cap][d]
+ * fp32 in expert-major order put back into receive order in back
+ * [rows_cap][d] fp32, ready for the combine all-to-all (which returns to
+ * each source the rows it sent, in the order it sent them). */
+moe_status moe_ep_regroup_back(const moe_config* cfg, int32_t n_ranks, int32_t rank,
+                               const int32_t* owner, const int32_t* kept_all,
+                               int64_t rows_cap, const float* o_local, float* back,
+                               moe_stats* stats, void* ws, moe_stream_t stream);
+
+/* Combine step, source device: the inverse of moe_ep_pack on the returned
+ * expert outputs: back [A_max][d] fp32 in send order put at their slots in
+ * o [A_max][d] fp32, so that moe_combine forms y exactly as on one device. */
+moe_status moe_ep_unpack(const moe_config* cfg, int32_t n_ranks, const int32_t* owner,
+                         const int32_t* offsets, const float* back, float* o,
+                         moe_stats* stats, void* ws, moe_stream_t stream);
 
 /* Tracing (instrumentation; the pages have no counterpart). Registers up to
  * 8 caller-created CUDA events (cudaEvent_t, passed as void*) for the

@@ -31,7 +31,8 @@ EXPORTED = ["moe_workspace_size", "moe_capacity", "moe_route", "moe_route_no_wor
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_status_string",
             "moe_backward", "moe_trace_events", "moe_selftest_bounded_wait",
             "moe_forward_launch_count", "moe_backward_launch_count",
-            "moe_ffn_uses_tensor_cores"]
+            "moe_ffn_uses_tensor_cores", "moe_ep_workspace_size", "moe_ep_pack",
+            "moe_ep_regroup", "moe_ep_regroup_back", "moe_ep_unpack"]
 
 
 class MoEError(RuntimeError):
@@ -112,8 +113,16 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_backward_launch_count.restype = ctypes.c_int32
     lib.moe_trace_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
     lib.moe_trace_events.restype = ctypes.c_int
+    lib.moe_ep_workspace_size.argtypes = [cfgp, ctypes.c_int32]
+    lib.moe_ep_workspace_size.restype = ctypes.c_size_t
+    i32, i64 = ctypes.c_int32, ctypes.c_int64
+    lib.moe_ep_pack.argtypes = [cfgp, i32, P, P, P, P, P, statp, P, P]
+    lib.moe_ep_regroup.argtypes = [cfgp, i32, i32, P, P, i64, P, P, P, statp, P, P]
+    lib.moe_ep_regroup_back.argtypes = [cfgp, i32, i32, P, P, i64, P, P, statp, P, P]
+    lib.moe_ep_unpack.argtypes = [cfgp, i32, P, P, P, P, statp, P, P]
     for name in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-                 "moe_backward"):
+                 "moe_backward", "moe_ep_pack", "moe_ep_regroup", "moe_ep_regroup_back",
+                 "moe_ep_unpack"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -305,10 +314,14 @@ def moe_route(cfg: LayerConfig, x, w_r, b_r, idx, gate, stats: Stats | None, ws,
 def moe_route_no_workspace(cfg: LayerConfig, x, w_r, b_r, idx, gate, stats: Stats | None,
                            stream=None):
     """moe_route without a workspace: for callers that cannot allocate device
-    memory. The library keeps the statistics' partial sums in a fixed 1 MiB
-    array (ceil(T/32) * N <= 131072); calls share it, so calls that overlap on
-    the GPU must not be issued. The first call on a device does a one-time
-    set-up; make it before any stream capture."""
+    memory. It always runs the CUDA-core router (moe_route takes the tensor-
+    core router for bf16 layers with d % 64 == 0, so the two can choose
+    differently on near-tie tokens). The library keeps the statistics'
+    partial sums in a fixed 1 MiB array (ceil(T/32) * (N + 2) <= 131072,
+    else MOE_ERR_WORKSPACE); calls share it, so calls that overlap on the GPU
+    must not be issued. The first call in a CUDA context (normally once per
+    device) looks up the array's address; make it before any stream
+    capture."""
     lib = load_library()
     st = stats.c() if stats is not None else None
     code = lib.moe_route_no_workspace(ctypes.byref(cfg.c()), _ptr(x), _ptr(w_r), _ptr(b_r),
@@ -556,3 +569,59 @@ class MoELayer:
                 laux_host[i:i + 1].copy_(p["stats"][b].l_aux, non_blocking=True)
                 out_done[b].record(p["s_out"])
         p["s_out"].synchronize()
+
+
+# --------------------------------------------------------------------------
+# expert-parallel staging (the layout around the two all-to-alls; the caller
+# exchanges the buffers with its own collective)
+# --------------------------------------------------------------------------
+def ep_workspace_size(cfg: LayerConfig, n_ranks: int) -> int:
+    return int(load_library().moe_ep_workspace_size(ctypes.byref(cfg.c()), int(n_ranks)))
+
+
+moe_ep_workspace_size = ep_workspace_size
+
+
+def alloc_ep_workspace(cfg: LayerConfig, n_ranks: int, device="cuda") -> torch.Tensor:
+    n = ep_workspace_size(cfg, n_ranks)
+    if n == 0:
+        raise MoEError(MOE_ERR_INVALID, "moe_ep_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _st(stats):
+    return ctypes.byref(stats.c()) if stats is not None else None
+
+
+def moe_ep_pack(cfg: LayerConfig, n_ranks: int, owner, offsets, x_perm, send, send_counts,
+                stats: Stats | None, ws, stream=None):
+    code = load_library().moe_ep_pack(ctypes.byref(cfg.c()), int(n_ranks), _ptr(owner),
+                                      _ptr(offsets), _ptr(x_perm), _ptr(send),
+                                      _ptr(send_counts), _st(stats), _ptr(ws), _stream(stream))
+    _check(code, "moe_ep_pack")
+
+
+def moe_ep_regroup(cfg: LayerConfig, n_ranks: int, rank: int, owner, kept_all, rows_cap: int,
+                   recv, x_local, local_offsets, stats: Stats | None, ws, stream=None):
+    code = load_library().moe_ep_regroup(ctypes.byref(cfg.c()), int(n_ranks), int(rank),
+                                         _ptr(owner), _ptr(kept_all), int(rows_cap), _ptr(recv),
+                                         _ptr(x_local), _ptr(local_offsets), _st(stats),
+                                         _ptr(ws), _stream(stream))
+    _check(code, "moe_ep_regroup")
+
+
+def moe_ep_regroup_back(cfg: LayerConfig, n_ranks: int, rank: int, owner, kept_all,
+                        rows_cap: int, o_local, back, stats: Stats | None, ws, stream=None):
+    code = load_library().moe_ep_regroup_back(ctypes.byref(cfg.c()), int(n_ranks), int(rank),
+                                              _ptr(owner), _ptr(kept_all), int(rows_cap),
+                                              _ptr(o_local), _ptr(back), _st(stats), _ptr(ws),
+                                              _stream(stream))
+    _check(code, "moe_ep_regroup_back")
+
+
+def moe_ep_unpack(cfg: LayerConfig, n_ranks: int, owner, offsets, back, o,
+                  stats: Stats | None, ws, stream=None):
+    code = load_library().moe_ep_unpack(ctypes.byref(cfg.c()), int(n_ranks), _ptr(owner),
+                                        _ptr(offsets), _ptr(back), _ptr(o), _st(stats),
+                                        _ptr(ws), _stream(stream))
+    _check(code, "moe_ep_unpack")
