@@ -20,6 +20,8 @@
 
 #include <float.h>
 
+#include <cuda.h>
+
 #include <mutex>
 
 namespace moe {
@@ -215,6 +217,68 @@ __global__ void route_laux_kernel(const float* __restrict__ psum, const int32_t*
   if (lane == 0) *l_aux = alpha * static_cast<float>(N) * s;
 }
 
+// With few partials ((N + 2) * nblk <= kStatsOneBlockMax) one block of 1024
+// threads reduces every row and then L_aux: one launch instead of two. Warp w
+// sums rows w, w + 32, ...: lane l adds partial blocks l, l + 32, ... in
+// order, then a fixed butterfly adds the lanes; L_aux adds f * P over the
+// experts as route_laux_kernel does. Fixed order, so deterministic.
+constexpr int64_t kStatsOneBlockMax = int64_t(1) << 18;
+
+__global__ void __launch_bounds__(1024)
+route_stats_one_block_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pcnt,
+                             int nblk, int T, int N, int K, float alpha, int32_t* count,
+                             float* f, float* P, float* z_loss, float* entropy, float* l_aux) {
+  __shared__ float tot[258];
+  __shared__ int32_t totc[256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  for (int r = warp; r < N + 2; r += nwarps) {
+    const bool expert = r < N;  // rows N, N+1: z-loss and entropy sums
+    const float* ps = psum + static_cast<size_t>(r) * nblk;
+    const int32_t* pc = pcnt + static_cast<size_t>(expert ? r : 0) * nblk;
+    float sum = 0.f;
+    int32_t c = 0;
+#pragma unroll 4
+    for (int b = lane; b < nblk; b += 32) {
+      sum += ps[b];
+      if (expert) c += pc[b];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    if (lane == 0) {
+      tot[r] = sum;
+      if (expert) totc[r] = c;
+    }
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < N + 2; r += blockDim.x) {
+    const float mean = T > 0 ? tot[r] / static_cast<float>(T) : 0.f;
+    if (r < N) {
+      if (count) count[r] = totc[r];
+      if (f) f[r] = T > 0 ? static_cast<float>(totc[r]) / (static_cast<float>(T) * K) : 0.f;
+      if (P) P[r] = mean;
+    } else {
+      float* dst = r == N ? z_loss : entropy;
+      if (dst) *dst = mean;
+    }
+  }
+  if (warp == 0 && l_aux != nullptr) {
+    float sum = 0.f;
+    for (int e = lane; e < N; e += 32) {
+      const float Pe = T > 0 ? tot[e] / static_cast<float>(T) : 0.f;
+      const float fe =
+          T > 0 ? static_cast<float>(totc[e]) / (static_cast<float>(T) * K) : 0.f;
+      sum += fe * Pe;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) *l_aux = alpha * static_cast<float>(N) * sum;
+  }
+}
+
 template <typename Tx>
 cudaError_t launch_router_t(const moe_config& c, const Tx* x, const float* w_r, const float* b_r,
                             int32_t* idx, float* gate, float* psum, int32_t* pcnt,
@@ -262,6 +326,12 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (st && (st->count || st->f || st->P || st->l_aux || st->z_loss || st->entropy)) {
+    if (static_cast<int64_t>(c.n_experts + 2) * nblk <= kStatsOneBlockMax) {
+      route_stats_one_block_kernel<<<1, 1024, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts,
+                                                      c.top_k, c.alpha, st->count, st->f,
+                                                      st->P, st->z_loss, st->entropy, st->l_aux);
+      return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
     route_stats_kernel<<<c.n_experts + 2, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts,
                                                        c.top_k, st->count, st->f, st->P,
                                                        st->z_loss, st->entropy);
@@ -275,6 +345,12 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
   return MOE_OK;
 }
 
+int route_stats_launches(const moe_config& c) {
+  const RouterTcPlan plan = router_tc_plan(c);
+  const int64_t nblk = plan.use ? plan.stat_blocks : (c.T + BM - 1) / BM;
+  return static_cast<int64_t>(c.n_experts + 2) * nblk <= kStatsOneBlockMax ? 1 : 2;
+}
+
 }  // namespace moe
 
 // ---------------------------------------------------------------------------
@@ -284,8 +360,12 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
 // serving process whose device memory is all owned by its own pool and that
 // forbids any other allocation after start-up, or a plug-in interface whose
 // signature has no workspace argument. For them moe_route_no_workspace runs
-// the same router and statistics kernels as moe_route, with the per-block
-// partial sums held in the fixed array below instead of the workspace. The
+// the CUDA-core (FFMA) router and the statistics kernels of moe_route, with
+// the per-block partial sums held in the fixed array below instead of the
+// workspace. moe_route takes the tensor-core router for bf16 layers whose d
+// is a multiple of 64; the two sum the logits in different orders, so their
+// choices can differ on near-tie tokens (an adjacent gap among the K+1
+// largest logits below 1e-5) and this entry point can be slower there. The
 // array lives in every GPU that loads this library, until the process exits.
 //
 // Limit: ceil(T / 32) * (N + 2) <= kRouteScratchElems (131072; 1 MiB of
@@ -304,24 +384,62 @@ namespace {
 constexpr size_t kRouteScratchElems = 131072;
 static __device__ __align__(256) unsigned char g_route_scratch[kRouteScratchElems * 8];
 
-// Device address of g_route_scratch on each device, looked up once per
-// device with that device current (in host code the symbol's name is only a
-// host-side stand-in, never a device address).
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+// Device address of g_route_scratch, looked up once per CUDA context with
+// that context current (in host code the symbol's name is only a host-side
+// stand-in, never a device address). A context belongs to one device, and
+// its ID (cuCtxGetId) is never reused within the process, so an address
+// cached under a context that was destroyed (cudaDeviceReset) or belongs to
+// another context on the same device is never handed out again. When the
+// driver's context calls are unavailable the address is looked up on every
+// call instead.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+constexpr int kScratchCache = 64;
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+ScratchEntry g_scratch_cache[kScratchCache] = {};
+int g_scratch_next = 0;
 std::mutex g_scratch_mu;
 
 moe_status route_scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  auto context_id = [](unsigned long long* id) {
+    CUcontext ctx = nullptr;
+    return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+           get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+  };
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
-      return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  unsigned long long id = 0;
+  if (context_id(&id))
+    for (const ScratchEntry& e : g_scratch_cache)
+      if (e.ctx_id == id) {
+        *out = e.addr;
+        return MOE_OK;
+      }
+  // the lookup also makes the device's primary context current when this
+  // thread has none yet; the key is read again after it
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+    return MOE_ERR_CUDA;
+  if (context_id(&id)) {
+    g_scratch_cache[g_scratch_next] = ScratchEntry{id, p};
+    g_scratch_next = (g_scratch_next + 1) % kScratchCache;
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return MOE_OK;
 }
 
