@@ -113,7 +113,39 @@ combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_of,
   }
 }
 
+// One warp per token: a token whose one assignment was dropped (slot -1)
+// gets y = x (residual) or 0; kept tokens are left to the fused down
+// projection.
+template <typename Tx>
+__global__ void __launch_bounds__(256)
+dropped_residual_kernel(const int32_t* __restrict__ slot_of, const Tx* __restrict__ x,
+                        Tx* __restrict__ y, int T, int d, int add_residual) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T || slot_of[t] >= 0) return;
+  const int lane = threadIdx.x & 31;
+  const int chunks = d * static_cast<int>(sizeof(Tx)) / 16;
+  uint4* dst = reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d);
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
+  for (int c = lane; c < chunks; c += 32)
+    dst[c] = add_residual ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
+
+moe_status launch_dropped_residual(const moe_config& c, const int32_t* slot_of, const void* x,
+                                   void* y, cudaStream_t s) {
+  if (c.T == 0) return MOE_OK;
+  const unsigned blocks = static_cast<unsigned>((c.T + 7) / 8);
+  if (c.dtype == MOE_BF16)
+    dropped_residual_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+        slot_of, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), c.T,
+        c.d_model, c.add_residual);
+  else
+    dropped_residual_kernel<float><<<blocks, 256, 0, s>>>(
+        slot_of, static_cast<const float*>(x), static_cast<float*>(y), c.T, c.d_model,
+        c.add_residual);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 moe_status launch_combine(const moe_config& c, const float* o, const int32_t* slot_of,
                           const float* gate, const void* x, void* y, cudaStream_t s) {

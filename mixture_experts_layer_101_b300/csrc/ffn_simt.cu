@@ -57,20 +57,37 @@ grouped_gemm_simt(const T* __restrict__ A, const T* __restrict__ B0, const T* __
   const T* Bb0 = B0 + static_cast<size_t>(e) * n_out * kdim;
   const T* Bb1 = (EPI == EPI_SWIGLU) ? B1 + static_cast<size_t>(e) * n_out * kdim : nullptr;
 
-  for (int k0 = 0; k0 < kdim; k0 += BK) {
-    // stage A (64 x 16) and B (64 x 16): 1024 elements each, 4 per thread
-    for (int i = threadIdx.x; i < BM * BK; i += kThreads) {
+  // A (64 x 16) and B (64 x 16) per K step: 1024 elements each, 4 per thread
+  // (element i = threadIdx.x + j * kThreads). The next step's elements are
+  // loaded into registers before this step's products, so their latency
+  // overlaps the arithmetic (small layers are latency-bound).
+  constexpr int PER = BM * BK / kThreads;
+  float ra[PER], rb0[PER], rb1[PER];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = threadIdx.x + j * kThreads;
       const int r = i / BK, kk = i % BK;
       const int k = k0 + kk;
-      As[kk][r] = (r < rows && k < kdim)
-                      ? to_f32(A[static_cast<size_t>(row0 + r) * kdim + k]) : 0.f;
+      ra[j] = (r < rows && k < kdim) ? to_f32(A[static_cast<size_t>(row0 + r) * kdim + k]) : 0.f;
       const int n = n0 + r;
-      Bs0[kk][r] = (n < n_out && k < kdim) ? to_f32(Bb0[static_cast<size_t>(n) * kdim + k]) : 0.f;
+      rb0[j] = (n < n_out && k < kdim) ? to_f32(Bb0[static_cast<size_t>(n) * kdim + k]) : 0.f;
       if (EPI == EPI_SWIGLU)
-        Bs1[kk][r] =
-            (n < n_out && k < kdim) ? to_f32(Bb1[static_cast<size_t>(n) * kdim + k]) : 0.f;
+        rb1[j] = (n < n_out && k < kdim) ? to_f32(Bb1[static_cast<size_t>(n) * kdim + k]) : 0.f;
+    }
+  };
+  fetch(0);
+  for (int k0 = 0; k0 < kdim; k0 += BK) {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = threadIdx.x + j * kThreads;
+      const int r = i / BK, kk = i % BK;
+      As[kk][r] = ra[j];
+      Bs0[kk][r] = rb0[j];
+      if (EPI == EPI_SWIGLU) Bs1[kk][r] = rb1[j];
     }
     __syncthreads();
+    if (k0 + BK < kdim) fetch(k0 + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float a[4], b0[4], b1[4];

@@ -86,6 +86,13 @@ struct TcArgs {
   float* part;             // ksplit > 1 the epilogue writes fp32 gate | up partials
   int64_t rows_part;       // part[ks][row][2F] (rows_part rows per part) and
                            // swiglu_combine_kernel applies SwiGLU
+  // down with the combine fused (one routed expert per token, no shared
+  // experts): y != NULL makes the epilogue write y[token] = g * o (+ x[token])
+  // in bf16 instead of o
+  const int32_t* token_of_slot;
+  const float* gate;       // [T] the token's gate
+  const __nv_bfloat16* xres;  // [T][d] residual rows or NULL
+  __nv_bfloat16* y;        // [T][d]
 };
 
 // silu(g) * u. The division is the fast reciprocal-multiply form (about two
@@ -116,7 +123,41 @@ __device__ __forceinline__ void store_pre(__nv_bfloat16* dst, int F, const uint3
   }
 }
 
-// MODE 0: gate/up + SwiGLU -> h (bf16). MODE 1: down -> o (fp32).
+// Fused combine of one row chunk: y[t][col .. col+32) = bf16(g * o (+ x)),
+// with the rounding steps of the combine kernel (the gate product rounded to
+// fp32, then the residual added in fp32, then one rounding to bf16), so the
+// result is the same bit for bit.
+__device__ __forceinline__ void store_y_chunk(const TcArgs& a, int t, float g, int col,
+                                              const uint32_t (&v)[32]) {
+  const size_t base = static_cast<size_t>(t) * a.ldo + col;
+  uint4 xr[4] = {};
+  if (a.xres != nullptr) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.xres + base);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) xr[q] = __ldg(src + q);
+  }
+  const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(xr);
+  uint32_t packed[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float a0 = __fmaf_rn(g, __uint_as_float(v[2 * j]), 0.f);
+    float a1 = __fmaf_rn(g, __uint_as_float(v[2 * j + 1]), 0.f);
+    if (a.xres != nullptr) {
+      const float2 xv = __bfloat1622float2(xh[j]);
+      a0 = __fadd_rn(a0, xv.x);
+      a1 = __fadd_rn(a1, xv.y);
+    }
+    __nv_bfloat162 b = __floats2bfloat162_rn(a0, a1);
+    packed[j] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.y + base);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+}
+
+// MODE 0: gate/up + SwiGLU -> h (bf16). MODE 1: down -> o (fp32), or y with
+// the combine fused.
 template <int MODE, int BNH>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -393,6 +434,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             n * Sh::OUT_COLS + c * 32,
                         args.ldo, g, u);
           }
+        }
+      } else if (args.y != nullptr) {
+        const int t = valid ? args.token_of_slot[grow] : 0;
+        const float g = valid ? args.gate[t] : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < Sh::BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          if (valid) store_y_chunk(args, t, g, n * Sh::OUT_COLS + c * 32, v);
         }
       } else {
         float* out = static_cast<float*>(args.out) + grow * args.ldo + n * Sh::OUT_COLS;
@@ -698,6 +749,16 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
                         args.ldo, g, u);
           }
         }
+      } else if (args.y != nullptr) {
+        const int t = valid ? args.token_of_slot[grow] : 0;
+        const float g = valid ? args.gate[t] : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          if (valid) store_y_chunk(args, t, g, n * 256 + c * 32, v);
+        }
       } else {
         float* out = static_cast<float*>(args.out) + grow * args.ldo + n * 256;
 #pragma unroll 1
@@ -903,7 +964,7 @@ bool ffn_tc_supported(const moe_config& c) {
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w, void* h, float* o,
                          void* pre, const int32_t* poff, float* gu_part, uint32_t* status,
-                         cudaStream_t s, int part) {
+                         cudaStream_t s, int part, const FusedCombine* fc) {
   if (rows == 0) return MOE_OK;
   const int E = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
   const bool pairs1 = use_pairs(c, rows, d);  // gate/up: reduction over d
@@ -919,7 +980,8 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
         !make_map(&mu, w.w_up, static_cast<uint64_t>(E) * F, d, 128))
       return MOE_ERR_CUDA;
     const int ksplit = pairs1 ? 1 : gate_up_ksplit(c, rows);
-    TcArgs a1{offsets, E, d, F / 128, F, h, F, status, pre, poff, ksplit, gu_part, rows};
+    TcArgs a1{offsets, E, d, F / 128, F, h, F, status, pre, poff, ksplit, gu_part, rows,
+              nullptr, nullptr, nullptr, nullptr};
     if (pairs1) {
       if (launch_pair<0>(mx, mg, mu, a1, ptiles * (F / 128), s) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -945,7 +1007,10 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
     if (!make_map(&mh, h, rows, F, 128) ||
         !make_map(&md, w.w_down, static_cast<uint64_t>(E) * d, F, pairs2 ? 128 : 256))
       return MOE_ERR_CUDA;
-    TcArgs a2{offsets, E, F, d / 256, d, o, d, status, nullptr, nullptr, 1, nullptr, rows};
+    TcArgs a2{offsets, E, F, d / 256, d, o, d, status, nullptr, nullptr, 1, nullptr, rows,
+              fc ? fc->token_of_slot : nullptr, fc ? fc->gate : nullptr,
+              fc ? static_cast<const __nv_bfloat16*>(fc->x) : nullptr,
+              fc ? static_cast<__nv_bfloat16*>(fc->y) : nullptr};
     if (pairs2) {
       if (launch_pair<1>(mh, md, md, a2, ptiles * (d / 256), s) != cudaSuccess)
         return MOE_ERR_CUDA;

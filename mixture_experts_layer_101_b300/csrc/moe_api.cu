@@ -200,7 +200,8 @@ void trace(int i, cudaStream_t s) { trace_record(i, s); }
 
 moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offsets,
                     const moe_expert_weights* w, float* o, moe_stats* stats, void* ws,
-                    cudaStream_t s, bool traced, bool keep_pre) {
+                    cudaStream_t s, bool traced, bool keep_pre,
+                    const FusedCombine* fc = nullptr) {
   const WsLayout L = ws_layout(c);
   void* h = at(ws, L.h);
   void* pre = keep_pre ? at(ws, L.pre) : nullptr;
@@ -215,12 +216,20 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
     const int64_t rows = rows_max_of(c);
     const moe_status r =
         tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, pre, poff,
-                           reinterpret_cast<float*>(at(ws, L.gu_part)), status, s, part)
+                           reinterpret_cast<float*>(at(ws, L.gu_part)), status, s, part, fc)
            : launch_ffn_simt(*c, rows, x_perm, offsets, *w, h, o, pre, s, part);
     if (r != MOE_OK) return r;
     if (traced) trace(2 + part, s);
   }
   return MOE_OK;
+}
+
+// moe_forward writes y from the down projection's epilogue (no fp32 o, no
+// combine pass) when each token has at most one expert output (K = 1 and no
+// shared experts) on the tensor-core path, and the backward pass does not
+// need o.
+bool combine_fused(const moe_config& c) {
+  return c.top_k == 1 && c.n_shared == 0 && c.save_for_backward == 0 && ffn_tc_supported(c);
 }
 
 }  // namespace
@@ -246,11 +255,11 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   const RouterTcPlan rp = router_tc_plan(*cfg);
   // tensor cores: weight split, GEMM (+ top-K unless fused); else one CUDA-core kernel
   const int router = rp.use ? (rp.fused ? 2 : 3) : 1;
-  const int stats = 2;                                  // per-expert reduction, L_aux
+  const int stats = route_stats_launches(*cfg);         // per-expert reduction (+ L_aux)
   const int dispatch = 4;                               // histogram, scan, permute, gather
   // gate/up (+ the SwiGLU of a split reduction), down
   const int ffn = 2 + (ffn_tc_supported(*cfg) && gate_up_ksplit(*cfg, rows_max_of(cfg)) > 1 ? 1 : 0);
-  const int combine = 1;
+  const int combine = 1;  // or, fused into the down projection, the dropped-token pass
   // keeping the pre-activations for the tensor-core backward: their padded offsets
   const int keep = cfg->save_for_backward && ffn_tc_supported(*cfg) ? 1 : 0;
   return router + stats + dispatch + ffn + combine + keep;
@@ -396,9 +405,16 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r, c
                         reinterpret_cast<int32_t*>(at(ws, L.gbase)), any ? &dst : nullptr, s);
     if (r != MOE_OK) return r;
     trace(2, s);
-    r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true, keep);
-    if (r != MOE_OK) return r;
-    r = launch_combine(*cfg, o, slot_of, gate, x, y, s);
+    if (combine_fused(*cfg)) {
+      const FusedCombine fc{tos, gate, cfg->add_residual ? x : nullptr, y};
+      r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true, keep, &fc);
+      if (r != MOE_OK) return r;
+      r = launch_dropped_residual(*cfg, slot_of, x, y, s);
+    } else {
+      r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true, keep);
+      if (r != MOE_OK) return r;
+      r = launch_combine(*cfg, o, slot_of, gate, x, y, s);
+    }
     trace(5, s);
     return r;
   } catch (...) {

@@ -129,6 +129,9 @@ struct RouterScratch {
 moe_status launch_router(const moe_config& c, const void* x, const float* w_r,
                          const float* b_r, int32_t* idx, float* gate, const RouterScratch& sc,
                          const moe_stats* st, cudaStream_t s);
+// Kernels launch_router uses to reduce the statistics partials (all of them
+// requested, the tensor-core router when the plan uses it): 1 or 2.
+int route_stats_launches(const moe_config& c);
 moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const void* x,
                             const float* w_r, const float* b_r, int32_t* idx, float* gate,
                             __nv_bfloat16* w3, float* part, float* psum, int32_t* pcnt,
@@ -141,6 +144,10 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
 
 moe_status launch_combine(const moe_config& c, const float* o, const int32_t* slot_of,
                           const float* gate, const void* x, void* y, cudaStream_t s);
+// With the combine fused into the down projection (K = 1, S = 0): y[t] = x[t]
+// (residual) or 0 for every token whose one assignment was dropped.
+moe_status launch_dropped_residual(const moe_config& c, const int32_t* slot_of, const void* x,
+                                   void* y, cudaStream_t s);
 
 // Expert FFN on CUDA cores (any dtype/shape) over the N + n_shared experts;
 // rows = rows of x_perm / h / o. part: 1 = gate/up (or the first Linear +
@@ -152,6 +159,16 @@ moe_status launch_ffn_simt(const moe_config& c, int64_t rows, const void* x_perm
 
 // Expert FFN on tcgen05 tensor cores (bf16, d % 256 == 0, F % 128 == 0).
 bool ffn_tc_supported(const moe_config& c);
+// The down projection writes y directly instead of o when every token has at
+// most one expert output (K = 1, no shared experts): y[token_of_slot[s]] =
+// bf16(gate[t] * o[s] (+ x[t])), the combine's arithmetic; the tokens the
+// capacity dropped are written by launch_dropped_residual.
+struct FusedCombine {
+  const int32_t* token_of_slot;
+  const float* gate;
+  const void* x;  // residual rows or NULL
+  void* y;
+};
 // pre (NULL or [padded rows][2F]) at rows poff[e] + r (the backward's padded
 // row space, each expert's rows rounded up to 64). gu_part: fp32 partials
 // [gate_up_ksplit][rows][2F] of a split gate/up reduction (decode-sized
@@ -160,7 +177,8 @@ int gate_up_ksplit(const moe_config& c, int64_t rows);
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w,
                          void* h, float* o, void* pre, const int32_t* poff, float* gu_part,
-                         uint32_t* status, cudaStream_t s, int part);
+                         uint32_t* status, cudaStream_t s, int part,
+                         const FusedCombine* fc = nullptr);
 // poff[e] = sum over e' < e of the rows of e' rounded up to 64 (one warp).
 moe_status launch_pad_offsets(const int32_t* offsets, int G, int32_t* poff, cudaStream_t s);
 
