@@ -58,9 +58,9 @@ import moe_inputs  # noqa: E402
 METRIC = "MoE-layer tokens/sec and % of roofline (TFLOP/s or HBM GB/s), 1×B300"
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the dominant kernel, from the ncu capture summarised in
-# profiles/grouped_gemm_mixtral_prefill.md, valid only while the kernel sources
-# hash to the recorded fingerprint (otherwise "traffic" is reported as null).
+# the dominant kernel, from an ncu capture of that kernel, valid only while
+# the kernel sources hash to the fingerprint recorded with it (otherwise
+# "traffic" is reported as null).
 KERNEL_SOURCES = ["mixture_experts_layer_101_b300/csrc/ffn_tc.cu",
                   "mixture_experts_layer_101_b300/csrc/ptx_sm100.cuh",
                   "mixture_experts_layer_101_b300/csrc/moe_common.cuh"]
@@ -241,13 +241,23 @@ def measured_peaks():
                 "source": "fallback"}
 
 
+def combine_fused(w) -> bool:
+    """Whether moe_forward writes y from the down projection's epilogue: one
+    expert output per token (K = 1, no shared experts) on the tensor-core path
+    (bf16 SwiGLU, d % 256 == 0, F % 128 == 0)."""
+    return (w.K == 1 and w.n_shared == 0 and w.dtype == "bf16" and w.activation == "swiglu"
+            and w.d % 256 == 0 and w.F % 128 == 0)
+
+
 def algorithmic_work(w, kept, offsets_active):
     """FLOPs and bytes the layer's definition needs (kept assignments only).
 
     gate/up GEMM: flops 2*A*d*(2F); bytes: the active experts' gate and up
     weights once, x_perm read once, h written once (bf16).
     down GEMM:    flops 2*A*F*d; bytes: active experts' down weights, h read,
-                  o written (fp32).
+                  o written (fp32); with the combine fused into it (K = 1, no
+                  shared experts) y written for the kept tokens instead (and
+                  their residual rows read).
     layer:        flops 2*A*d*F*mats; bytes: active experts' weights once, x
                   read once, y written once, the router weights."""
     A = int(kept)
@@ -258,7 +268,10 @@ def algorithmic_work(w, kept, offsets_active):
     gu_flops = 2.0 * A * d * F * (2 if w.activation == "swiglu" else 1)
     gu_bytes = act * (mats - 1) * F * d * es + A * d * es + A * F * es
     dn_flops = 2.0 * A * F * d
-    dn_bytes = act * F * d * es + A * F * es + A * d * 4
+    if combine_fused(w):
+        dn_bytes = act * F * d * es + A * F * es + A * d * es * (2 if w.add_residual else 1)
+    else:
+        dn_bytes = act * F * d * es + A * F * es + A * d * 4
     layer_flops = gu_flops + dn_flops
     layer_bytes = act * mats * F * d * es + 2 * w.T * d * es + w.N * d * 4
     return {"gate_up": (gu_flops, gu_bytes), "down": (dn_flops, dn_bytes),
@@ -730,6 +743,128 @@ def run_train(args, world, rank):
     return 0
 
 
+def ep_bytes(rows_src, rows_dst, d, es):
+    """Bytes each expert-parallel staging call reads plus writes: pack and
+    unpack move the source device's kept rows (x in the layer dtype, expert
+    outputs in fp32), regroup and regroup back the rows a device receives."""
+    return {"ep_pack": 2 * rows_src * d * es, "ep_unpack": 2 * rows_src * d * 4,
+            "ep_regroup": 2 * rows_dst * d * es, "ep_regroup_back": 2 * rows_dst * d * 4}
+
+
+def run_ep(args, world, rank):
+    """Expert-parallel staging on one device: the source side (pack of the
+    dispatched rows by destination, unpack of the returned fp32 outputs) and
+    the destination side of device 0 (regroup of what it receives by expert,
+    regroup back of its outputs), with args.ep_ranks devices holding the
+    experts in blocks and every source routing like this one. The exchange
+    itself is not part of the library and not timed."""
+    import mixture_experts_layer_101_b300 as moe
+
+    moe.load_library()
+    w = selected_workload(args)
+    if w.n_shared:
+        raise SystemExit("--pass ep: shared experts are not exchanged")
+    R = args.ep_ranks
+    cfg = moe.LayerConfig.from_workload(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = moe_inputs.make_x(w).to(dev)
+    w_r, b_r = moe_inputs.make_router(w)
+    N, K, d = w.N, w.K, w.d
+    ws = moe.alloc_workspace(cfg, dev)
+    st = moe.Stats(N, dev)
+    A = max(moe.a_max(cfg), 1)
+    idx = torch.empty((w.T, K), dtype=torch.int32, device=dev)
+    gate = torch.empty((w.T, K), dtype=torch.float32, device=dev)
+    moe.moe_route(cfg, x, w_r.to(dev), None if b_r is None else b_r.to(dev), idx, gate, st, ws)
+    offsets = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    slot_of = torch.empty((w.T, K), dtype=torch.int32, device=dev)
+    tos = torch.empty(A, dtype=torch.int32, device=dev)
+    x_perm = torch.empty((A, d), dtype=cfg.torch_dtype, device=dev)
+    moe.moe_dispatch(cfg, x, idx, offsets, slot_of, tos, x_perm, st, ws)
+    torch.cuda.synchronize()
+    owner_h = [e * R // N for e in range(N)]
+    owner = torch.tensor(owner_h, dtype=torch.int32, device=dev)
+    kept = st.kept.clone()
+    kept_all = kept.unsqueeze(0).repeat(R, 1).contiguous()
+    rows_src = int(kept.sum())
+    rows_dst = R * int(sum(int(kept[e]) for e in range(N) if owner_h[e] == 0))
+    cap = max(rows_dst, 1)
+    g = torch.Generator(device=dev).manual_seed(7)
+    send = torch.empty((A, d), dtype=cfg.torch_dtype, device=dev)
+    counts = torch.empty(R, dtype=torch.int32, device=dev)
+    back = torch.randn((A, d), generator=g, device=dev)
+    o = torch.empty((A, d), dtype=torch.float32, device=dev)
+    recv = torch.randn((cap, d), generator=g, device=dev).to(cfg.torch_dtype)
+    x_local = torch.empty((cap, d), dtype=cfg.torch_dtype, device=dev)
+    loff = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    o_local = torch.randn((cap, d), generator=g, device=dev)
+    back_local = torch.empty((cap, d), dtype=torch.float32, device=dev)
+    ws_ep = moe.alloc_ep_workspace(cfg, R, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    calls = {
+        "ep_pack": lambda: moe.moe_ep_pack(cfg, R, owner, offsets, x_perm, send, counts, st,
+                                           ws_ep),
+        "ep_regroup": lambda: moe.moe_ep_regroup(cfg, R, 0, owner, kept_all, cap, recv, x_local,
+                                                 loff, st, ws_ep),
+        "ep_regroup_back": lambda: moe.moe_ep_regroup_back(cfg, R, 0, owner, kept_all, cap,
+                                                           o_local, back_local, st, ws_ep),
+        "ep_unpack": lambda: moe.moe_ep_unpack(cfg, R, owner, offsets, back, o, st, ws_ep),
+    }
+    for _ in range(args.warmup):
+        for f in calls.values():
+            f()
+    torch.cuda.synchronize()
+    st.status.zero_()
+    names = list(calls)
+    ms = {n: [] for n in names}
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler() as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+            flush.fill_(i & 0xFF)
+            ev[0].record()
+            for j, n in enumerate(names):
+                calls[n]()
+                ev[j + 1].record()
+            torch.cuda.synchronize()
+            for j, n in enumerate(names):
+                ms[n].append(ev[j].elapsed_time(ev[j + 1]))
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    if st.status_bits() != 0:
+        raise SystemExit(f"device status word {st.status_bits():#x} after the timed steps")
+    es = 2 if w.dtype == "bf16" else 4
+    nbytes = ep_bytes(rows_src, rows_dst, d, es)
+    mean_s = {n: statistics.mean(v) / 1e3 for n, v in ms.items()}
+    step_s = sum(mean_s.values())
+    max_s = max_over_ranks(step_s * args.steps, world)
+    rows = 2 * rows_src + 2 * rows_dst
+    value = sum_over_ranks(float(rows * args.steps), world) / max_s
+    peaks = measured_peaks()
+    dominant = max(names, key=lambda n: mean_s[n])
+    roof = roofline_entry(0.0, nbytes[dominant], mean_s[dominant], peaks)
+    roof.update(kernel=dominant, traffic=None, peak_source=f"{peaks['source']} HBM copy")
+    per_call = {n: {"ms": round(mean_s[n] * 1e3, 4), "bytes": nbytes[n],
+                    "gbs": round(nbytes[n] / mean_s[n] / 1e9, 1),
+                    "frac": round(nbytes[n] / mean_s[n] / 1e9 / peaks["hbm_gbs"], 4)}
+                for n in names}
+    if rank == 0:
+        line = {"metric": "EP staging rows/s (pack, regroup, regroup back, unpack), 1xB300",
+                "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "config": workload_config(w, args, {"ep_ranks": R, "placement": "block",
+                                                    "source_rows": rows_src,
+                                                    "received_rows": rows_dst}),
+                "roofline": roof, "calls": per_call, "gpu_launches": 8 * args.steps,
+                "clocks": clocks.summary(), "wall_s_timed_region": round(wall, 4)}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -749,8 +884,12 @@ def main(argv=None):
     ap.add_argument("--eager", dest="graph", action="store_false",
                     help="launch every kernel per step instead of replaying the step as one "
                          "captured CUDA graph (the default)")
-    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "train"],
-                    help="forward (the layer's metric) or train: forward + backward")
+    ap.add_argument("--pass", dest="pass_", default="forward",
+                    choices=["forward", "train", "ep"],
+                    help="forward (the layer's metric), train: forward + backward, or ep: the "
+                         "expert-parallel staging calls")
+    ap.add_argument("--ep-ranks", type=int, default=8,
+                    help="devices holding the experts (--pass ep)")
     ap.add_argument("--z-coef", type=float, default=1e-3,
                     help="z-loss weight in the training objective (--pass train)")
     ap.add_argument("--select-bias", action="store_true",
@@ -764,6 +903,8 @@ def main(argv=None):
             return run_reference(args, world, rank)
         if args.pass_ == "train":
             return run_train(args, world, rank)
+        if args.pass_ == "ep":
+            return run_ep(args, world, rank)
         return run_ours(args, world, rank)
     finally:
         if world > 1:

@@ -34,6 +34,17 @@ def test_inactive_experts_cost_no_weight_bytes():
     assert a - b == 32 * 2 * w.F * w.d * 2
 
 
+def test_switch_down_with_the_combine_fused():
+    # K = 1, no shared experts: the down projection writes the kept tokens' y
+    # (bf16) and reads their residual rows instead of writing fp32 o
+    w = moe_inputs.WORKLOADS["switch_skewed"]
+    assert bench.combine_fused(w)
+    dn_b = bench.algorithmic_work(w, 12316, 64)["down"][1]
+    assert dn_b == 64 * 1024 * 4096 * 2 + 12316 * 4096 * 2 + 12316 * 1024 * 2 * 2
+    assert not bench.combine_fused(moe_inputs.WORKLOADS["mixtral_prefill"])   # K = 2
+    assert not bench.combine_fused(moe_inputs.WORKLOADS["tiny_fp32"])         # CUDA cores
+
+
 def test_backward_work_is_twice_the_forward_flops():
     w = moe_inputs.WORKLOADS["mixtral_prefill"]
     bw = bench.backward_work(w, 8192, 8)
@@ -130,3 +141,13 @@ def test_reference_arm_json_line():
     assert j["cpu_baseline"]["value"] == j["value"]
     assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_ep_staging_bytes():
+    # 8192 kept rows leave the source; device 0 of 8 (one expert each)
+    # receives 8 * 1000 rows; d = 4096 in bf16, outputs in fp32
+    b = bench.ep_bytes(8192, 8000, 4096, 2)
+    assert b["ep_pack"] == 2 * 8192 * 4096 * 2
+    assert b["ep_unpack"] == 2 * 8192 * 4096 * 4
+    assert b["ep_regroup"] == 2 * 8000 * 4096 * 2
+    assert b["ep_regroup_back"] == 2 * 8000 * 4096 * 4
