@@ -801,8 +801,11 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
 // Gate/up with a split reduction: h[r][f] = silu(g) * u with g, u the sums of
 // the parts' fp32 partials in ascending part order (the same SwiGLU as the
 // GEMM epilogue); with pre, (g, u) rounded to bf16 are kept at padded row
-// poff[e] + (r - offsets[e]). Block r handles row r (rows past offsets[E]
-// have no data and return).
+// poff[e] + (r - offsets[e]). Block (r, c) handles columns [512 c, 512 c + 512)
+// of row r, two per thread (rows past offsets[E] have no data and return), so
+// a decode-sized batch of a few dozen rows still fills the GPU.
+constexpr int kSwigluCols = 512;
+
 __global__ void __launch_bounds__(256)
 swiglu_combine_kernel(const float* __restrict__ part, int ksplit, int64_t rows_part,
                       const int32_t* __restrict__ offsets, int E, int F,
@@ -820,7 +823,9 @@ swiglu_combine_kernel(const float* __restrict__ part, int ksplit, int64_t rows_p
     }
     prow = poff[lo] + (r - offsets[lo]);
   }
-  for (int f = threadIdx.x * 2; f < F; f += blockDim.x * 2) {
+  const int f_end = min(F, static_cast<int>(blockIdx.y + 1) * kSwigluCols);
+  for (int f = static_cast<int>(blockIdx.y) * kSwigluCols + threadIdx.x * 2; f < f_end;
+       f += blockDim.x * 2) {
     float2 g = make_float2(0.f, 0.f), u = make_float2(0.f, 0.f);
     for (int ks = 0; ks < ksplit; ++ks) {
       const float* row = part + (static_cast<size_t>(ks) * rows_part + r) * 2 * F;
@@ -995,7 +1000,8 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                                 TcShape<0, 128>::SMEM, s>>>(mx, mg, mu, mx64, mx32, mx16, a1);
       if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
       if (ksplit > 1) {
-        swiglu_combine_kernel<<<static_cast<unsigned>(rows), 256, 0, s>>>(
+        const dim3 grid(static_cast<unsigned>(rows), (F + kSwigluCols - 1) / kSwigluCols);
+        swiglu_combine_kernel<<<grid, 256, 0, s>>>(
             gu_part, ksplit, rows, offsets, E, F, static_cast<__nv_bfloat16*>(h),
             static_cast<__nv_bfloat16*>(pre), poff);
         if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
