@@ -75,10 +75,12 @@ combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_of,
       xr[tt] = (add_residual && t < T) ? R::load(x + static_cast<size_t>(t) * d + c) : R::zero();
     }
   };
-  const int c0 = threadIdx.x * 4;
+  // block column slice y of gridDim.y (one slice unless the batch is small)
+  const int c0 = (static_cast<int>(blockIdx.y) * kThreads + threadIdx.x) * 4;
+  const int cstride = kThreads * 4 * static_cast<int>(gridDim.y);
   if (c0 < d) load_residual(c0);
   __syncthreads();
-  for (int c = c0; c < d; c += kThreads * 4) {
+  for (int c = c0; c < d; c += cstride) {
     if (c != c0) load_residual(c);
     float4 acc[TPB];
 #pragma unroll
@@ -150,9 +152,15 @@ moe_status launch_dropped_residual(const moe_config& c, const int32_t* slot_of, 
 moe_status launch_combine(const moe_config& c, const float* o, const int32_t* slot_of,
                           const float* gate, const void* x, void* y, cudaStream_t s) {
   if (c.T == 0) return MOE_OK;
-  const bool wide = c.top_k + c.n_shared <= 2;
+  // A small batch (fewer token blocks than twice the SMs) takes one token per
+  // block and splits the columns over blockIdx.y, so its few rows still
+  // spread over many SMs (decode: 16 tokens in 64 blocks instead of 4).
+  const int cols_per_block = kThreads * 4;
+  const bool small = c.T < 2 * sm_count();
+  const bool wide = c.top_k + c.n_shared <= 2 && !small;
   const int tpb = wide ? 4 : 1;
-  const unsigned blocks = static_cast<unsigned>((c.T + tpb - 1) / tpb);
+  const int slices = small ? (c.d_model + cols_per_block - 1) / cols_per_block : 1;
+  const dim3 blocks(static_cast<unsigned>((c.T + tpb - 1) / tpb), static_cast<unsigned>(slices));
 #define MOE_COMBINE(TX, TPBV)                                                                  \
   combine_kernel<TX, TPBV><<<blocks, kThreads, 0, s>>>(o, slot_of, gate,                       \
                                                        static_cast<const TX*>(x),              \

@@ -151,8 +151,9 @@ dispatch_permute_kernel(const int32_t* __restrict__ idx, int T, int K, int N, in
   }
 }
 
-// x_perm[s] = x[token_of_slot[s]] for s < offsets[N]: one warp per slot, 16
-// bytes per lane per step, four steps in flight.
+// x_perm[s] = x[token_of_slot[s]] for s < offsets[N]: one warp per slot and
+// column slice (blockIdx.y of gridDim.y: one slice unless the batch is small),
+// 16 bytes per lane per step, four steps in flight.
 template <typename Tx>
 __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ token_of_slot,
@@ -164,9 +165,12 @@ dispatch_gather_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ tok
   const int lane = threadIdx.x & 31;
   // routed slots come from the permutation; shared slots hold the tokens in order
   const int t = slot < routed ? token_of_slot[slot] : (slot - routed) % T;
-  const int chunks = d * static_cast<int>(sizeof(Tx)) / 16;
-  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
-  uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(slot) * d);
+  const int all = d * static_cast<int>(sizeof(Tx)) / 16;
+  const int per = (all + gridDim.y - 1) / gridDim.y;
+  const int c0 = min(all, static_cast<int>(blockIdx.y) * per);
+  const int chunks = min(all, c0 + per) - c0;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d) + c0;
+  uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(slot) * d) + c0;
   int c = lane;
   for (; c + 96 < chunks; c += 128) {
     const uint4 a = __ldg(src + c), b = __ldg(src + c + 32), e = __ldg(src + c + 64),
@@ -184,7 +188,7 @@ dispatch_gather_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ tok
 moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* offsets, int32_t* slot_of, int32_t* token_of_slot,
                            void* x_perm, int32_t* ghist, int32_t* gbase, const moe_stats* st,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool gather_rows) {
   const int N = c.n_experts, K = c.top_k;
   const int32_t C = capacity_of(&c);
   uint32_t* status = st ? st->status : nullptr;
@@ -202,8 +206,12 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
                                                              offsets, slot_of, token_of_slot);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     const int64_t rows = rows_max_of(&c);
-    const unsigned gblocks = static_cast<unsigned>((rows + 7) / 8);
-    if (gblocks > 0) {
+    // few rows (decode): split each row's columns over blockIdx.y, 4 KB a slice
+    const int row_bytes = c.d_model * (c.dtype == MOE_BF16 ? 2 : 4);
+    const unsigned slices =
+        rows < 2 * sm_count() ? static_cast<unsigned>((row_bytes + 4095) / 4096) : 1u;
+    const dim3 gblocks(static_cast<unsigned>((rows + 7) / 8), slices);
+    if (rows > 0 && gather_rows) {
       if (c.dtype == MOE_BF16)
         dispatch_gather_kernel<__nv_bfloat16><<<gblocks, 256, 0, s>>>(
             static_cast<const __nv_bfloat16*>(x), token_of_slot, offsets, N, c.n_shared, c.T,

@@ -63,21 +63,33 @@ struct Shape {
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, NPT);
 };
 
+// Four consecutive weights per thread (d % 64 == 0 on this path): one
+// 16-byte load, one 8-byte store per plane.
 __global__ void __launch_bounds__(256)
 router_split_kernel(const float* __restrict__ w_r, int N, int NP, int d,
                     __nv_bfloat16* __restrict__ w3) {
   const size_t total = static_cast<size_t>(NP) * d;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t e = i / d;
-    const float w = e < static_cast<size_t>(N) ? w_r[i] : 0.f;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    w3[i] = hi;
-    w3[total + i] = mid;
-    w3[2 * total + i] = __float2bfloat16_rn(r2);
+  for (size_t i = (blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x) * 4; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x * 4) {
+    const size_t e = i / d;  // the four weights share a row: d % 4 == 0
+    const float4 w4 = e < static_cast<size_t>(N) ? __ldg(reinterpret_cast<const float4*>(w_r + i))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float w[4] = {w4.x, w4.y, w4.z, w4.w};
+    uint32_t bits[3][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(w[j]);
+      const float r1 = w[j] - __bfloat162float(hi);
+      const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+      const float r2 = r1 - __bfloat162float(mid);
+      bits[0][j] = __bfloat16_as_ushort(hi);
+      bits[1][j] = __bfloat16_as_ushort(mid);
+      bits[2][j] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+    }
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+      *reinterpret_cast<uint2*>(w3 + q * total + i) =
+          make_uint2(bits[q][0] | (bits[q][1] << 16), bits[q][2] | (bits[q][3] << 16));
   }
 }
 
