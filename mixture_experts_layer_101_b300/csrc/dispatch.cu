@@ -188,7 +188,7 @@ dispatch_gather_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ tok
 moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* offsets, int32_t* slot_of, int32_t* token_of_slot,
                            void* x_perm, int32_t* ghist, int32_t* gbase, const moe_stats* st,
-                           cudaStream_t s, bool gather_rows) {
+                           cudaStream_t s) {
   const int N = c.n_experts, K = c.top_k;
   const int32_t C = capacity_of(&c);
   uint32_t* status = st ? st->status : nullptr;
@@ -211,7 +211,7 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
     const unsigned slices =
         rows < 2 * sm_count() ? static_cast<unsigned>((row_bytes + 4095) / 4096) : 1u;
     const dim3 gblocks(static_cast<unsigned>((rows + 7) / 8), slices);
-    if (rows > 0 && gather_rows) {
+    if (rows > 0) {
       if (c.dtype == MOE_BF16)
         dispatch_gather_kernel<__nv_bfloat16><<<gblocks, 256, 0, s>>>(
             static_cast<const __nv_bfloat16*>(x), token_of_slot, offsets, N, c.n_shared, c.T,
