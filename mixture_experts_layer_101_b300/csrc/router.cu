@@ -199,30 +199,41 @@ route_stats_kernel(float* __restrict__ psum, int32_t* __restrict__ pcnt, int nbl
 }
 
 // L_aux = alpha * N * sum_e f[e] * P[e] from the per-expert totals that
-// route_stats_kernel left in psum[e][0], pcnt[e][0]. One warp: lane l adds
-// experts l, l+32, ... in order, then a fixed butterfly adds the lanes.
-__global__ void route_laux_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pcnt,
-                                  int nblk, int T, int N, int K, float alpha, float* l_aux) {
-  const int lane = threadIdx.x & 31;
+// route_stats_kernel left in psum[e][0], pcnt[e][0]. One thread per expert
+// loads its two totals (all loads in flight at once); warp w then adds the
+// products of experts 32w .. 32w+31 with a fixed butterfly and thread 0 adds
+// the warps in order.
+__global__ void __launch_bounds__(256)
+route_laux_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pcnt, int nblk,
+                  int T, int N, int K, float alpha, float* l_aux) {
+  __shared__ float wsum[8];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
   float s = 0.f;
-  for (int e = lane; e < N; e += 32) {
-    const float Pe = T > 0 ? psum[static_cast<size_t>(e) * nblk] / static_cast<float>(T) : 0.f;
-    const float fe = T > 0 ? static_cast<float>(pcnt[static_cast<size_t>(e) * nblk]) /
-                                 (static_cast<float>(T) * K)
-                           : 0.f;
-    s += fe * Pe;
+  if (e < N && T > 0) {
+    const float Pe = psum[static_cast<size_t>(e) * nblk] / static_cast<float>(T);
+    const float fe = static_cast<float>(pcnt[static_cast<size_t>(e) * nblk]) /
+                     (static_cast<float>(T) * K);
+    s = fe * Pe;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) *l_aux = alpha * static_cast<float>(N) * s;
+  if (lane == 0) wsum[warp] = s;
+  __syncthreads();
+  if (e == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += wsum[w];
+    *l_aux = alpha * static_cast<float>(N) * t;
+  }
 }
 
-// With few partials ((N + 2) * nblk <= kStatsOneBlockMax) one block of 1024
+// With at most 32 partial blocks per row (small batches) one block of 1024
 // threads reduces every row and then L_aux: one launch instead of two. Warp w
-// sums rows w, w + 32, ...: lane l adds partial blocks l, l + 32, ... in
-// order, then a fixed butterfly adds the lanes; L_aux adds f * P over the
-// experts as route_laux_kernel does. Fixed order, so deterministic.
-constexpr int64_t kStatsOneBlockMax = int64_t(1) << 18;
+// sums rows w, w + 32, ...: lane l takes partial block l, then a fixed
+// butterfly adds the lanes; L_aux adds f * P over the experts in a fixed
+// order. With more partial blocks a warp would walk them serially (measured:
+// 15 us for 256 per row, 78 us for 512 rows of 258, latency-bound), so the
+// per-row blocks of route_stats_kernel take them instead.
+constexpr int kStatsOneBlockMaxBlocks = 32;
 
 __global__ void __launch_bounds__(1024)
 route_stats_one_block_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pcnt,
@@ -326,7 +337,7 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (st && (st->count || st->f || st->P || st->l_aux || st->z_loss || st->entropy)) {
-    if (static_cast<int64_t>(c.n_experts + 2) * nblk <= kStatsOneBlockMax) {
+    if (nblk <= kStatsOneBlockMaxBlocks) {
       route_stats_one_block_kernel<<<1, 1024, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts,
                                                       c.top_k, c.alpha, st->count, st->f,
                                                       st->P, st->z_loss, st->entropy, st->l_aux);
@@ -337,8 +348,8 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
                                                        st->z_loss, st->entropy);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     if (st->l_aux) {
-      route_laux_kernel<<<1, 32, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k, c.alpha,
-                                         st->l_aux);
+      route_laux_kernel<<<1, 256, 0, s>>>(psum, pcnt, nblk, c.T, c.n_experts, c.top_k, c.alpha,
+                                          st->l_aux);
       if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }
   }
@@ -348,7 +359,7 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
 int route_stats_launches(const moe_config& c) {
   const RouterTcPlan plan = router_tc_plan(c);
   const int64_t nblk = plan.use ? plan.stat_blocks : (c.T + BM - 1) / BM;
-  return static_cast<int64_t>(c.n_experts + 2) * nblk <= kStatsOneBlockMax ? 1 : 2;
+  return nblk <= kStatsOneBlockMaxBlocks ? 1 : 2;
 }
 
 }  // namespace moe
