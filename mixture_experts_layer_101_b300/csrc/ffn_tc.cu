@@ -909,6 +909,21 @@ bool use_pairs(const moe_config& c, int64_t rows, int kdim) {
   return rows >= static_cast<int64_t>(c.n_experts + c.n_shared) * BM * 4 && kdim >= 1024;
 }
 
+// The down projection also takes CTA pairs when experts have about one row
+// tile each, as long as its pair tiles fill the clusters at least twice:
+// measured on the DeepSeek-shaped layer (128 rows per expert, F = 2048) the
+// down GEMM went 1.90 -> 1.55 ms on pairs (a pair's odd CTA reads no
+// activation rows there and stores nothing; each SM streams half a weight
+// tile per K step), while its gate/up GEMM got slower on pairs (2.57 -> 2.86
+// ms). Decode-sized batches (too few pair tiles) stay on one CTA per tile.
+bool down_uses_pairs(const moe_config& c, int64_t rows) {
+  if (use_pairs(c, rows, c.d_ff)) return true;
+  if (c.d_ff < 1024) return false;
+  const int64_t E = c.n_experts + c.n_shared;
+  const int64_t pair_tiles = (E + (rows + 2 * BM - 1) / (2 * BM)) * (c.d_model / 256);
+  return pair_tiles >= sm_count();  // two per cluster of two SMs
+}
+
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const TcArgs& args, int64_t pair_tiles, cudaStream_t s) {
@@ -973,7 +988,7 @@ moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
   if (rows == 0) return MOE_OK;
   const int E = c.n_experts + c.n_shared, d = c.d_model, F = c.d_ff;  // routed + shared
   const bool pairs1 = use_pairs(c, rows, d);  // gate/up: reduction over d
-  const bool pairs2 = use_pairs(c, rows, F);  // down: reduction over F
+  const bool pairs2 = down_uses_pairs(c, rows);  // down: reduction over F
   if (!set_smem_attr()) return MOE_ERR_CUDA;
   const int64_t mtiles = E + (rows + BM - 1) / BM;       // upper bound on (expert, m-tile)
   const int64_t ptiles = E + (rows + 2 * BM - 1) / (2 * BM);

@@ -48,6 +48,9 @@ SMALL = {
     "tc_pairs_both": wl(T=1500, d=2048, F=2048, N=2, K=2),
     "tc_pairs_shared_capacity": wl(T=2048, d=1024, F=2048, N=2, K=1, n_shared=1,
                                    capacity_factor=1.5, add_residual=True),
+    # about a dozen rows per expert but enough pair tiles: the down projection
+    # runs on CTA pairs (odd CTAs past their expert's rows), gate/up on one CTA
+    "tc_down_pairs_small_experts": wl(T=512, d=2048, F=1024, N=64, K=2),
     # K = 1, pairs: the down projection's pair epilogue writes y (combine fused)
     "tc_pairs_top1_capacity": wl(T=2048, d=1024, F=2048, N=2, K=1, capacity_factor=0.9,
                                  add_residual=True, router_bias="uniform"),
