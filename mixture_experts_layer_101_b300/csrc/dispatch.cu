@@ -52,7 +52,8 @@ constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads)
 dispatch_scan_kernel(const int32_t* __restrict__ ghist, int nq, int N, int32_t C, int S, int T,
                      int32_t* __restrict__ gbase, int32_t* __restrict__ offsets,
-                     int32_t* count, int32_t* kept_out, int32_t* n_dropped) {
+                     int32_t* count, int32_t* kept_out, int32_t* n_dropped,
+                     int32_t* sched_zero) {
   __shared__ int32_t run_sum[kScanThreads];
   __shared__ int32_t kept[256], cnt[256];
   const int tid = threadIdx.x;
@@ -104,6 +105,7 @@ dispatch_scan_kernel(const int32_t* __restrict__ ghist, int nq, int N, int32_t C
     }
     const int32_t total = __shfl_sync(0xffffffffu, inc, 31);
     if (tid == 0) {
+      if (sched_zero) sched_zero[0] = sched_zero[1] = 0;  // the expert GEMMs' tile counters
       offsets[N] = total;
       for (int s2 = 0; s2 < S; ++s2) offsets[N + s2 + 1] = total + (s2 + 1) * T;  // shared experts
       if (n_dropped) *n_dropped = ds;
@@ -188,7 +190,7 @@ dispatch_gather_kernel(const Tx* __restrict__ x, const int32_t* __restrict__ tok
 moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* offsets, int32_t* slot_of, int32_t* token_of_slot,
                            void* x_perm, int32_t* ghist, int32_t* gbase, const moe_stats* st,
-                           cudaStream_t s) {
+                           cudaStream_t s, int32_t* sched_zero) {
   const int N = c.n_experts, K = c.top_k;
   const int32_t C = capacity_of(&c);
   uint32_t* status = st ? st->status : nullptr;
@@ -199,7 +201,8 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
   }
   dispatch_scan_kernel<<<1, kScanThreads, 0, s>>>(
       ghist, c.T > 0 ? K * nb : 0, N, C, c.n_shared, c.T, gbase, offsets,
-      st ? st->count : nullptr, st ? st->kept : nullptr, st ? st->n_dropped : nullptr);
+      st ? st->count : nullptr, st ? st->kept : nullptr, st ? st->n_dropped : nullptr,
+      sched_zero);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   if (c.T > 0) {
     dispatch_permute_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, c.n_shared, C, gbase,

@@ -104,6 +104,7 @@ WsLayout ws_layout(const moe_config* c) {
   L.o = take(A * d * 4);
   const int ks = ffn_tc_supported(*c) ? gate_up_ksplit(*c, static_cast<int64_t>(A)) : 1;
   L.gu_part = take(ks > 1 ? static_cast<size_t>(ks) * A * 2 * F * 4 : 0);
+  L.sched = take(2 * 4);
   const bool bw = c->save_for_backward != 0;
   // router-gradient K splits: about 1024 tokens each, at most 32
   L.rsplits = bw ? static_cast<int>(std::min<size_t>(32, std::max<size_t>(1, T / 1024))) : 0;
@@ -200,7 +201,7 @@ void trace(int i, cudaStream_t s) { trace_record(i, s); }
 
 moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offsets,
                     const moe_expert_weights* w, float* o, moe_stats* stats, void* ws,
-                    cudaStream_t s, bool traced, bool keep_pre,
+                    cudaStream_t s, bool traced, bool keep_pre, bool sched_zeroed,
                     const FusedCombine* fc = nullptr) {
   const WsLayout L = ws_layout(c);
   void* h = at(ws, L.h);
@@ -216,7 +217,9 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
     const int64_t rows = rows_max_of(c);
     const moe_status r =
         tc ? launch_ffn_tc(*c, rows, x_perm, offsets, *w, h, o, pre, poff,
-                           reinterpret_cast<float*>(at(ws, L.gu_part)), status, s, part, fc)
+                           reinterpret_cast<float*>(at(ws, L.gu_part)),
+                           reinterpret_cast<int32_t*>(at(ws, L.sched)), sched_zeroed, status,
+                           s, part, fc)
            : launch_ffn_simt(*c, rows, x_perm, offsets, *w, h, o, pre, s, part);
     if (r != MOE_OK) return r;
     if (traced) trace(2 + part, s);
@@ -347,7 +350,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
     if (moe_status s = check_weights(cfg, weights)) return s;
     if (moe_status s = check_ws(cfg, ws)) return s;
     return ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws,
-                    static_cast<cudaStream_t>(stream), false, false);
+                    static_cast<cudaStream_t>(stream), false, false, false);
   } catch (...) {
     return MOE_ERR_CUDA;
   }
@@ -402,16 +405,17 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* w_r, c
     const bool any = dst.count || dst.kept || dst.n_dropped || dst.status;
     r = launch_dispatch(*cfg, x, idx, offsets, slot_of, tos, x_perm,
                         reinterpret_cast<int32_t*>(at(ws, L.ghist)),
-                        reinterpret_cast<int32_t*>(at(ws, L.gbase)), any ? &dst : nullptr, s);
+                        reinterpret_cast<int32_t*>(at(ws, L.gbase)), any ? &dst : nullptr, s,
+                        reinterpret_cast<int32_t*>(at(ws, L.sched)));
     if (r != MOE_OK) return r;
     trace(2, s);
     if (combine_fused(*cfg)) {
       const FusedCombine fc{tos, gate, cfg->add_residual ? x : nullptr, y};
-      r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true, keep, &fc);
+      r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true, keep, true, &fc);
       if (r != MOE_OK) return r;
       r = launch_dropped_residual(*cfg, slot_of, x, y, s);
     } else {
-      r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true, keep);
+      r = ffn_impl(cfg, x_perm, offsets, weights, o, stats, ws, s, true, keep, true);
       if (r != MOE_OK) return r;
       r = launch_combine(*cfg, o, slot_of, gate, x, y, s);
     }

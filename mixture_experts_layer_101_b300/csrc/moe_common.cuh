@@ -69,6 +69,7 @@ struct WsLayout {
   size_t o;                   // [A_max][d] fp32 (moe_forward only); the backward
                               // pass reuses it for the expert input gradients
   size_t gu_part;             // [ksplit][R_max][2F] fp32 split gate/up partials (decode)
+  size_t sched;               // [2] int32 tile counters of the CTA-pair GEMMs (gate/up, down)
   // save_for_backward only (size 0 otherwise):
   size_t logits;              // [T][N] fp32 router logits
   size_t pre;                 // [R_max][2F] dtype: SwiGLU gate | up pre-activations
@@ -140,7 +141,8 @@ moe_status launch_router_tc(const moe_config& c, const RouterTcPlan& p, const vo
 moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* offsets, int32_t* slot_of, int32_t* token_of_slot,
                            void* x_perm, int32_t* ghist, int32_t* gbase,
-                           const moe_stats* st, cudaStream_t s);
+                           const moe_stats* st, cudaStream_t s,
+                           int32_t* sched_zero = nullptr);  // [2] zeroed by the scan, or NULL
 
 moe_status launch_combine(const moe_config& c, const float* o, const int32_t* slot_of,
                           const float* gate, const void* x, void* y, cudaStream_t s);
@@ -172,13 +174,17 @@ struct FusedCombine {
 // pre (NULL or [padded rows][2F]) at rows poff[e] + r (the backward's padded
 // row space, each expert's rows rounded up to 64). gu_part: fp32 partials
 // [gate_up_ksplit][rows][2F] of a split gate/up reduction (decode-sized
-// batches; NULL when gate_up_ksplit(c, rows) == 1).
+// batches; NULL when gate_up_ksplit(c, rows) == 1). sched: two int32 tile
+// counters that the CTA-pair GEMMs claim tiles from (gate/up, down); they
+// must be 0 when each such GEMM starts: sched_zeroed says an earlier kernel
+// on the stream (the dispatch scan) zeroed both, otherwise each part zeroes
+// its counter before its launch.
 int gate_up_ksplit(const moe_config& c, int64_t rows);
 moe_status launch_ffn_tc(const moe_config& c, int64_t rows, const void* x_perm,
                          const int32_t* offsets, const moe_expert_weights& w,
                          void* h, float* o, void* pre, const int32_t* poff, float* gu_part,
-                         uint32_t* status, cudaStream_t s, int part,
-                         const FusedCombine* fc = nullptr);
+                         int32_t* sched, bool sched_zeroed, uint32_t* status, cudaStream_t s,
+                         int part, const FusedCombine* fc = nullptr);
 // poff[e] = sum over e' < e of the rows of e' rounded up to 64 (one warp).
 moe_status launch_pad_offsets(const int32_t* offsets, int G, int32_t* poff, cudaStream_t s);
 

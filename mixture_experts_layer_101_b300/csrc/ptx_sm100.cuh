@@ -218,6 +218,25 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
+// Asynchronous 32-bit store into the shared memory of a cluster CTA (addresses
+// from map_to_rank); its completion counts 4 transaction bytes on that CTA's
+// mbarrier bar_cluster, whose waiters then see the value. It does not wait
+// for, or order, the issuing thread's earlier memory operations.
+__device__ __forceinline__ void st_async_remote_u32(uint32_t cluster_addr, uint32_t v,
+                                                    uint32_t bar_cluster) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+          cluster_addr),
+      "r"(v), "r"(bar_cluster)
+      : "memory");
+}
+// Arrive on a cluster CTA's mbarrier without release semantics: nothing the
+// issuing thread did before is ordered by it (a release at cluster scope can
+// wait for the thread's outstanding memory operations).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
