@@ -153,6 +153,108 @@ dispatch_permute_kernel(const int32_t* __restrict__ idx, int T, int K, int N, in
   }
 }
 
+// Batches of at most 256 tokens (one token block): histogram, capacity scan
+// and permute in one block of 256 threads, one token per thread, with the
+// multi-block kernels' arithmetic: pass 1 counts each expert's assignments
+// over all ranks; warp 0 scans the kept counts into the offsets; pass 2 walks
+// the ranks k = 0 .. K-1 in order, where an assignment's rank within its
+// expert is the expert's count over the earlier ranks, plus the earlier warps'
+// counts at this rank, plus the earlier lanes of its warp with the same expert
+// (warp match). Same slots, bit for bit, in one launch instead of three.
+__global__ void __launch_bounds__(kThreads)
+dispatch_small_kernel(const int32_t* __restrict__ idx, int T, int K, int N, int S, int32_t C,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ slot_of,
+                      int32_t* __restrict__ token_of_slot, int32_t* count, int32_t* kept_out,
+                      int32_t* n_dropped, int32_t* sched_zero, uint32_t* status) {
+  __shared__ int32_t tot[256], kept[256], off[256], base[256];
+  __shared__ int32_t wcnt[kThreads / 32][256];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = tid;
+  tot[tid] = 0;
+  base[tid] = 0;
+  __syncthreads();
+  for (int k = 0; k < K; ++k) {
+    if (t < T) {
+      const int e = idx[static_cast<size_t>(t) * K + k];
+      if (e >= 0 && e < N) atomicAdd(&tot[e], 1);
+      else set_status(status, MOE_ERR_INDEX);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the kept counts over the experts
+    const int per_lane = (N + 31) / 32;
+    const int e0 = min(N, lane * per_lane), e1 = min(N, e0 + per_lane);
+    int32_t ks = 0, ds = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int32_t kp = tot[e] < C ? tot[e] : C;
+      kept[e] = kp;
+      ks += kp;
+      ds += tot[e] - kp;
+    }
+    int32_t inc = ks;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ds += __shfl_xor_sync(0xffffffffu, ds, o);
+    int32_t run = inc - ks;
+    for (int e = e0; e < e1; ++e) {
+      off[e] = run;
+      offsets[e] = run;
+      run += kept[e];
+    }
+    const int32_t total = __shfl_sync(0xffffffffu, inc, 31);
+    if (lane == 0) {
+      if (sched_zero) sched_zero[0] = sched_zero[1] = 0;  // the expert GEMMs' tile counters
+      offsets[N] = total;
+      for (int s2 = 0; s2 < S; ++s2) offsets[N + s2 + 1] = total + (s2 + 1) * T;
+      if (n_dropped) *n_dropped = ds;
+    }
+  }
+  for (int e = tid; e < N; e += kThreads) {
+    if (count) count[e] = tot[e];
+    if (kept_out) kept_out[e] = tot[e] < C ? tot[e] : C;
+  }
+  __syncthreads();
+  const int KS = K + S;
+  for (int k = 0; k < K; ++k) {
+    for (int i = tid; i < (kThreads / 32) * 256; i += kThreads) (&wcnt[0][0])[i] = 0;
+    int e = -1;
+    if (t < T) e = idx[static_cast<size_t>(t) * K + k];
+    const bool valid = (t < T) && e >= 0 && e < N;
+    const int key = valid ? e : N + lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const int rank_w = __popc(peers & ((1u << lane) - 1u));
+    __syncthreads();
+    if (valid && rank_w == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    int32_t slot = -1;
+    if (valid) {
+      int32_t rank = base[e] + rank_w;
+      for (int w = 0; w < warp; ++w) rank += wcnt[w][e];
+      if (rank < C) {
+        slot = off[e] + rank;
+        token_of_slot[slot] = t;
+      }
+    }
+    if (t < T) slot_of[static_cast<size_t>(t) * KS + k] = slot;
+    __syncthreads();
+    for (int e2 = tid; e2 < N; e2 += kThreads) {
+      int32_t add = 0;
+      for (int w = 0; w < kThreads / 32; ++w) add += wcnt[w][e2];
+      base[e2] += add;
+    }
+    __syncthreads();
+  }
+  if (t < T) {
+    const int32_t routed = offsets[N];
+    for (int s2 = 0; s2 < S; ++s2)
+      slot_of[static_cast<size_t>(t) * KS + K + s2] = routed + s2 * T + t;
+  }
+}
+
 // x_perm[s] = x[token_of_slot[s]] for s < offsets[N]: one warp per slot and
 // column slice (blockIdx.y of gridDim.y: one slice unless the batch is small),
 // 16 bytes per lane per step, four steps in flight.
@@ -195,19 +297,28 @@ moe_status launch_dispatch(const moe_config& c, const void* x, const int32_t* id
   const int32_t C = capacity_of(&c);
   uint32_t* status = st ? st->status : nullptr;
   const int nb = (c.T + kThreads - 1) / kThreads;
-  if (c.T > 0) {
-    dispatch_hist_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, ghist, status);
+  if (nb == 1) {
+    dispatch_small_kernel<<<1, kThreads, 0, s>>>(
+        idx, c.T, K, N, c.n_shared, C, offsets, slot_of, token_of_slot, st ? st->count : nullptr,
+        st ? st->kept : nullptr, st ? st->n_dropped : nullptr, sched_zero, status);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    if (c.T > 0) {
+      dispatch_hist_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, ghist, status);
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    dispatch_scan_kernel<<<1, kScanThreads, 0, s>>>(
+        ghist, c.T > 0 ? K * nb : 0, N, C, c.n_shared, c.T, gbase, offsets,
+        st ? st->count : nullptr, st ? st->kept : nullptr, st ? st->n_dropped : nullptr,
+        sched_zero);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (c.T > 0) {
+      dispatch_permute_kernel<<<dim3(nb, K), kThreads, 0, s>>>(
+          idx, c.T, K, N, c.n_shared, C, gbase, offsets, slot_of, token_of_slot);
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
   }
-  dispatch_scan_kernel<<<1, kScanThreads, 0, s>>>(
-      ghist, c.T > 0 ? K * nb : 0, N, C, c.n_shared, c.T, gbase, offsets,
-      st ? st->count : nullptr, st ? st->kept : nullptr, st ? st->n_dropped : nullptr,
-      sched_zero);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   if (c.T > 0) {
-    dispatch_permute_kernel<<<dim3(nb, K), kThreads, 0, s>>>(idx, c.T, K, N, c.n_shared, C, gbase,
-                                                             offsets, slot_of, token_of_slot);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     const int64_t rows = rows_max_of(&c);
     // few rows (decode): split each row's columns over blockIdx.y, 4 KB a slice
     const int row_bytes = c.d_model * (c.dtype == MOE_BF16 ? 2 : 4);

@@ -82,7 +82,8 @@ WsLayout ws_layout(const moe_config* c) {
   const size_t T = static_cast<size_t>(c->T), K = c->top_k, N = c->n_experts;
   const size_t d = c->d_model, F = c->d_ff, es = dtype_size(c);
   L.a_max = a_max_of(c);
-  L.nblk_r = static_cast<int>((T + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock);
+  L.nblk_r = router_small(*c) ? static_cast<int>(T)
+                              : static_cast<int>((T + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock);
   L.nblk_d = static_cast<int>((T + kDispatchTokensPerBlock - 1) / kDispatchTokensPerBlock);
   const size_t nr = L.nblk_r > 0 ? L.nblk_r : 1, nd = L.nblk_d > 0 ? L.nblk_d : 1;
   const size_t A = static_cast<size_t>(rows_max_of(c));  // routed + shared rows
@@ -256,10 +257,13 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   if (!config_valid(cfg, nullptr)) return -1;
   if (cfg->T == 0) return 1;  // the dispatch scan still writes offsets and counts
   const RouterTcPlan rp = router_tc_plan(*cfg);
-  // tensor cores: weight split, GEMM (+ top-K unless fused); else one CUDA-core kernel
-  const int router = rp.use ? (rp.fused ? 2 : 3) : 1;
+  // decode-sized batches or no tensor cores: one CUDA-core kernel; else the
+  // weight split and the GEMM (+ top-K unless fused)
+  const int router = router_small(*cfg) || !rp.use ? 1 : (rp.fused ? 2 : 3);
   const int stats = route_stats_launches(*cfg);         // per-expert reduction (+ L_aux)
-  const int dispatch = 4;                               // histogram, scan, permute, gather
+  // histogram, scan, permute, gather; at most 256 tokens: the one-block
+  // dispatch and the gather
+  const int dispatch = cfg->T <= kDispatchTokensPerBlock ? 2 : 4;
   // gate/up (+ the SwiGLU of a split reduction), down
   const int ffn = 2 + (ffn_tc_supported(*cfg) && gate_up_ksplit(*cfg, rows_max_of(cfg)) > 1 ? 1 : 0);
   const int combine = 1;  // or, fused into the down projection, the dropped-token pass

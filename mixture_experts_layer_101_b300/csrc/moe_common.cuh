@@ -57,7 +57,8 @@ constexpr int kDispatchTokensPerBlock = 256; // tokens per dispatch block
 struct WsLayout {
   size_t idx, gate;           // [T][K] int32 / fp32 (moe_forward only)
   size_t psum, pcnt;          // router partials [N+2][nblk_r], [N][nblk_r] (expert-major);
-                              // nblk_r = ceil(T / kTopkTokensPerBlock) covers every router
+                              // nblk_r = ceil(T / kTopkTokensPerBlock), or T for the
+                              // small-batch router, covers every router
   size_t w3, part;            // tensor-core router: W_r split [3][NP][d] bf16,
                               // partial logits [S][T][NP] fp32
   size_t ghist, gbase;        // dispatch histograms [K][nblk_d][N]
@@ -127,6 +128,9 @@ struct RouterScratch {
   float* part;
   float* logits;
 };
+// Decode-sized batches take the one-launch CUDA-core router (one block per
+// token; statistics partials per token, nblk = T).
+bool router_small(const moe_config& c);
 moe_status launch_router(const moe_config& c, const void* x, const float* w_r,
                          const float* b_r, int32_t* idx, float* gate, const RouterScratch& sc,
                          const moe_stats* st, cudaStream_t s);

@@ -226,14 +226,14 @@ route_laux_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pc
   }
 }
 
-// With at most 32 partial blocks per row (small batches) one block of 1024
+// With at most 64 partial blocks per row (small batches) one block of 1024
 // threads reduces every row and then L_aux: one launch instead of two. Warp w
-// sums rows w, w + 32, ...: lane l takes partial block l, then a fixed
-// butterfly adds the lanes; L_aux adds f * P over the experts in a fixed
-// order. With more partial blocks a warp would walk them serially (measured:
-// 15 us for 256 per row, 78 us for 512 rows of 258, latency-bound), so the
-// per-row blocks of route_stats_kernel take them instead.
-constexpr int kStatsOneBlockMaxBlocks = 32;
+// sums rows w, w + 32, ...: lane l takes partial blocks l and l + 32, then a fixed butterfly adds the lanes; L_aux adds f * P over the
+// experts in a fixed order. With many more partial blocks a warp would walk
+// them serially (measured: 15 us for 256 per row, 78 us for 512 rows of 258,
+// latency-bound), so the per-row blocks of route_stats_kernel take them
+// instead.
+constexpr int kStatsOneBlockMaxBlocks = 64;
 
 __global__ void __launch_bounds__(1024)
 route_stats_one_block_kernel(const float* __restrict__ psum, const int32_t* __restrict__ pcnt,
@@ -290,6 +290,107 @@ route_stats_one_block_kernel(const float* __restrict__ psum, const int32_t* __re
   }
 }
 
+// Decode-sized batches (router_small: T <= 128, N <= 32): one block of 8
+// warps per token. Warp w takes the w-th eighth of d (whole groups of four);
+// each lane keeps one fp32 partial per expert over its share, a
+// reduce-scatter across the warp (full butterfly steps over the offsets >= NE,
+// then halving steps in which the lanes with bit o set keep the upper half)
+// leaves lane l with the warp's partial for expert l % NE, and warp 0 adds the
+// eight warps' partials in order, adds b_r and runs the shared selection. One
+// launch replaces the tensor-core router's weight split, split-K GEMM and
+// top-K kernel, whose fixed costs exceed the work at this size. The
+// statistics partials are per token (nblk = T).
+template <typename Tx, int NE>
+__global__ void __launch_bounds__(kThreads)
+router_small_kernel(const Tx* __restrict__ x, const float* __restrict__ w_r,
+                    const float* __restrict__ b_r, const float* __restrict__ sel_bias,
+                    int gate_mode, int T, int d, int N, int K, int32_t* __restrict__ idx_out,
+                    float* __restrict__ gate_out, float* __restrict__ psum,
+                    int32_t* __restrict__ pcnt, uint32_t* __restrict__ status,
+                    float* __restrict__ logits_out) {
+  __shared__ float red[kWarps][32];
+  __shared__ float pw[kWarps][256];
+  __shared__ float zh[2 * kWarps];
+  __shared__ int32_t scnt[256];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.x;
+  for (int i = tid; i < 256; i += kThreads) scnt[i] = 0;
+
+  float acc[NE];
+#pragma unroll
+  for (int e = 0; e < NE; ++e) acc[e] = 0.f;
+  const int slice = ((d / 4 + kWarps - 1) / kWarps) * 4;
+  const int kb = min(d, warp * slice), ke = min(d, kb + slice);
+  const Tx* xr = x + static_cast<size_t>(t) * d;
+  // two groups of four per lane in flight (four, fully unrolled, measured
+  // slower on the decode-shaped router: 14.1 -> 16.4 us)
+#pragma unroll 2
+  for (int k = kb + lane * 4; k < ke; k += 128) {
+    const float4 xv = load4(xr + k);
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+      if (e < N) {
+        const float4 wv = load4(w_r + static_cast<size_t>(e) * d + k);
+        float a = acc[e];
+        a = fmaf(xv.x, wv.x, a);
+        a = fmaf(xv.y, wv.y, a);
+        a = fmaf(xv.z, wv.z, a);
+        a = fmaf(xv.w, wv.w, a);
+        acc[e] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= NE; o >>= 1)
+#pragma unroll
+    for (int e = 0; e < NE; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+#pragma unroll
+  for (int o = NE / 2; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? acc[i] : acc[i + o];
+      const float keep = upper ? acc[i + o] : acc[i];
+      acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  if (lane < NE) red[warp][lane] = acc[0];
+  __syncthreads();
+
+  float pacc[1] = {0.f};
+  float zacc = 0.f, hacc = 0.f;
+  if (warp == 0) {
+    float v[1] = {-INFINITY};
+    if (lane < N) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) s += red[w][lane];
+      if (b_r != nullptr) s += b_r[lane];
+      v[0] = s;
+    }
+    route_one_token<1>(v, N, K, static_cast<size_t>(t), lane, sel_bias, gate_mode, idx_out,
+                       gate_out, pacc, zacc, hacc, scnt, status, logits_out);
+  }
+  write_block_stats<1>(pacc, zacc, hacc, pw, zh, scnt, N, blockIdx.x, psum, pcnt);
+}
+
+template <typename Tx>
+cudaError_t launch_router_small(const moe_config& c, const Tx* x, const float* w_r,
+                                const float* b_r, int32_t* idx, float* gate, float* psum,
+                                int32_t* pcnt, uint32_t* status, float* logits, cudaStream_t s) {
+  const int N = c.n_experts;
+#define MOE_SMALL(NE)                                                                         \
+  router_small_kernel<Tx, NE><<<c.T, kThreads, 0, s>>>(x, w_r, b_r, c.select_bias,            \
+                                                       c.gate_mode, c.T, c.d_model, N,        \
+                                                       c.top_k, idx, gate, psum, pcnt,        \
+                                                       status, logits)
+  if (N <= 8) MOE_SMALL(8);
+  else if (N <= 16) MOE_SMALL(16);
+  else MOE_SMALL(32);
+#undef MOE_SMALL
+  return cudaGetLastError();
+}
+
 template <typename Tx>
 cudaError_t launch_router_t(const moe_config& c, const Tx* x, const float* w_r, const float* b_r,
                             int32_t* idx, float* gate, float* psum, int32_t* pcnt,
@@ -321,7 +422,16 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
   int32_t* pcnt = sc.pcnt;
   const RouterTcPlan plan = router_tc_plan(c);
   int nblk = (c.T + BM - 1) / BM;  // statistics partials left by the router
-  if (plan.use && sc.w3 != nullptr && (plan.fused || sc.part != nullptr)) {
+  if (router_small(c)) {
+    nblk = c.T;
+    const cudaError_t err =
+        c.dtype == MOE_BF16
+            ? launch_router_small(c, static_cast<const __nv_bfloat16*>(x), w_r, b_r, idx, gate,
+                                  psum, pcnt, status, sc.logits, s)
+            : launch_router_small(c, static_cast<const float*>(x), w_r, b_r, idx, gate, psum,
+                                  pcnt, status, sc.logits, s);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (plan.use && sc.w3 != nullptr && (plan.fused || sc.part != nullptr)) {
     nblk = plan.stat_blocks;
     const moe_status r = launch_router_tc(c, plan, x, w_r, b_r, idx, gate, sc.w3, sc.part, psum,
                                           pcnt, status, sc.logits, s);
@@ -356,9 +466,14 @@ moe_status launch_router(const moe_config& c, const void* x, const float* w_r, c
   return MOE_OK;
 }
 
+bool router_small(const moe_config& c) {
+  return c.T > 0 && c.T <= 128 && c.n_experts <= 32 && c.d_model % 4 == 0;
+}
+
 int route_stats_launches(const moe_config& c) {
   const RouterTcPlan plan = router_tc_plan(c);
-  const int64_t nblk = plan.use ? plan.stat_blocks : (c.T + BM - 1) / BM;
+  const int64_t nblk =
+      router_small(c) ? c.T : (plan.use ? plan.stat_blocks : (c.T + BM - 1) / BM);
   return nblk <= kStatsOneBlockMaxBlocks ? 1 : 2;
 }
 

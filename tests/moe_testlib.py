@@ -103,13 +103,16 @@ def expert_reader(experts: dict):
     return lambda e: {k: v[e].cpu() for k, v in experts.items()}
 
 
-def run_stages(cfg: moe.LayerConfig, inp: dict) -> dict:
-    """route -> dispatch -> expert_ffn -> combine through the C ABI."""
+def run_stages(cfg: moe.LayerConfig, inp: dict, ws_fill: int | None = None) -> dict:
+    """route -> dispatch -> expert_ffn -> combine through the C ABI (with
+    ws_fill, every workspace byte is set to it first)."""
     dev = "cuda"
     T, K, N, d = cfg.T, cfg.top_k, cfg.n_experts, cfg.d_model
     S = cfg.n_shared
     A = moe.rows_max(cfg)
     ws = moe.alloc_workspace(cfg)
+    if ws_fill is not None:
+        ws.fill_(ws_fill)
     st = moe.Stats(N)
     idx = torch.full((T, K), -7, dtype=torch.int32, device=dev)
     gate = torch.zeros((T, K), dtype=torch.float32, device=dev)

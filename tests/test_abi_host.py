@@ -121,20 +121,23 @@ def test_status_strings(lib):
 
 def test_launch_count(lib):
     # router (tensor cores: weight split, GEMM, top-K; fused: split, GEMM;
-    # CUDA cores: one kernel), statistics (one block while every row has at
-    # most 32 partial blocks, else per-row reduction + L_aux), dispatch (4),
-    # the two expert GEMMs, the combine
+    # CUDA cores, or T <= 128 with N <= 32: one kernel), statistics (one block
+    # while every row has at most 64 partial blocks, else per-row reduction +
+    # L_aux), dispatch (4; at most 256 tokens: 2), the two expert GEMMs, the
+    # combine
     assert moe.forward_launch_count(cfg()) == 12          # tensor-core router
     assert moe.forward_launch_count(cfg(dtype="f32")) == 10
     assert moe.forward_launch_count(cfg(d_model=72)) == 10  # d % 64 != 0: CUDA-core router
     assert moe.forward_launch_count(cfg(top_k=9, n_experts=16)) == -1
     # one K split and one expert tile: selection runs in the router GEMM epilogue
     assert moe.forward_launch_count(cfg(T=32768, d_model=1024, n_experts=64, top_k=1)) == 11
-    assert moe.forward_launch_count(cfg(T=100, d_model=64)) == 10  # one partial block
+    # small-batch router: one block and one statistics partial per token
+    assert moe.forward_launch_count(cfg(T=100, d_model=64)) == 8  # 100 partials: two kernels
+    assert moe.forward_launch_count(cfg(T=64, d_model=64)) == 7   # 64 partials: one block
     assert moe.forward_launch_count(cfg(T=4096, n_experts=256, top_k=8)) == 12  # two tiles
-    # decode: two partial blocks (one statistics kernel); the split gate/up
-    # reduction adds its SwiGLU pass
-    assert moe.forward_launch_count(cfg(T=16)) == 12
+    # decode: the small-batch router, 16 partials (one statistics kernel); the
+    # split gate/up reduction adds its SwiGLU pass
+    assert moe.forward_launch_count(cfg(T=16)) == 8
     assert moe.forward_launch_count(cfg(T=1 << 24, d_model=64, n_experts=8, top_k=2)) == 11
 
 

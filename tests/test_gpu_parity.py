@@ -67,6 +67,12 @@ SMALL = {
     # gate variants: full-softmax (Switch) gates, top-K selection bias
     "tc_softmax_gate": wl(T=300, d=256, F=256, N=8, K=2, gate_mode="softmax"),
     "tc_select_bias": wl(T=500, d=256, F=128, N=16, K=4, select_bias="uniform"),
+    # the small-batch router (T <= 128, N <= 32) with its 16- and 32-expert
+    # warp layouts, a selection bias, a router bias and softmax gates
+    "small_router_n12_selbias": wl(T=96, d=512, F=128, N=12, K=3, select_bias="uniform",
+                                   router_bias="uniform"),
+    "small_router_n32_softmax": wl(T=128, d=1024, F=256, N=32, K=4, gate_mode="softmax",
+                                   router_bias="skew"),
     "tc_switch_gate_capacity": wl(T=1000, d=256, F=128, N=8, K=1, gate_mode="softmax",
                                   capacity_factor=1.25, add_residual=True),
     # K = 1 without the residual: dropped tokens come out as zeros
@@ -155,6 +161,25 @@ def test_forward_equals_stages_and_is_deterministic(name):
     for k in ("count", "kept", "f", "P"):
         assert np.array_equal(st1[k], st2[k]) and np.array_equal(st1[k], gpu["stats"][k])
     assert st1["l_aux"] == st2["l_aux"] == gpu["stats"]["l_aux"]
+
+
+# The workspace is scratch: what it holds before a call must not change the
+# result. Every byte 0xA5 makes, among others, the tile counters of the
+# CTA-pair GEMMs large and negative; moe_forward (in the dispatch scan) and
+# moe_expert_ffn (before each pair launch) zero them.
+@pytest.mark.parametrize("name", ["tc_pairs_top1_capacity", "tc_pairs_shared_capacity",
+                                  "tc_down_pairs_small_experts", "tc_ragged"])
+def test_stale_workspace_does_not_change_results(name):
+    w = SMALL[name]
+    cfg = moe.LayerConfig.from_workload(w)
+    inp = L.device_inputs(w)
+    y_ref, _ = L.run_forward(cfg, inp)
+    layer = moe.MoELayer(cfg, inp["w_r"], inp["b_r"], inp["experts"])
+    layer.ws.fill_(0xA5)
+    y = layer.forward(inp["x"]).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu(), y_ref.cpu())
+    assert torch.equal(L.run_stages(cfg, inp, ws_fill=0xA5)["y"], L.run_stages(cfg, inp)["y"])
 
 
 def test_tensor_core_path_is_selected():
