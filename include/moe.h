@@ -194,14 +194,15 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* w_r,
  * no counterpart: this is an interface variant, not a different method).
  * A serving process whose device memory is all owned by its own pool, or a
  * plug-in interface that passes no workspace, can call this instead of
- * moe_route. It always runs the CUDA-core (FFMA) router and the statistics
+ * moe_route. It always runs a CUDA-core (FFMA) router and the statistics
  * kernels of moe_route, with the per-block partial sums of the statistics in
  * a fixed array inside the library (1 MiB, held on every GPU that loads the
  * library until the process exits) instead of a caller workspace. Nothing is
  * allocated: no cudaMalloc, no cudaFree.
- *   Results: those of moe_route, except that for bf16 layers with
- *   d % 64 == 0 moe_route takes the tensor-core router, which sums the logits
- *   in another order: the choice can then differ on near-tie tokens (some
+ *   Results: those of moe_route (for at most 128 tokens and 32 experts both
+ *   run the same small-batch router), except that for larger bf16 layers
+ *   with d % 64 == 0 moe_route takes the tensor-core router, which sums the
+ *   logits in another order: the choice can then differ on near-tie tokens (some
  *   adjacent gap among the K+1 largest logits below 1e-5), and this call can
  *   be slower on those layers.
  *   Limit: ceil(T / 32) * (N + 2) <= 131072 (e.g. T <= 16256 with N = 256,
