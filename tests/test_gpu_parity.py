@@ -59,6 +59,11 @@ SMALL = {
     # capacity (expert counts 1012 1009 1027 1048; the same capped at 1024;
     # 1435 1415 1407 1453 245 189)
     "tc_pair_tails_mixed": wl(T=2048, d=1024, F=1024, N=4, K=2, router_bias="uniform"),
+    # CTA pairs at 512 rows per expert on average, and with a capacity of 640,
+    # skewed routing and drops (the Switch-shaped layer's regime, smaller)
+    "tc_pairs_512_rows": wl(T=2048, d=1024, F=1024, N=4, K=1),
+    "tc_pairs_capacity_skew": wl(T=4096, d=1024, F=512, N=8, K=1, capacity_factor=1.25,
+                                 router_bias="skew", add_residual=True),
     "tc_pair_tails_exact": wl(T=2048, d=1024, F=1024, N=4, K=2, router_bias="uniform",
                               capacity_factor=1.0, add_residual=True),
     "tc_pair_tails_k3": wl(T=2048, d=1024, F=1024, N=6, K=3, router_bias="skew"),
