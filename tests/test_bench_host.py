@@ -151,3 +151,18 @@ def test_ep_staging_bytes():
     assert b["ep_unpack"] == 2 * 8192 * 4096 * 4
     assert b["ep_regroup"] == 2 * 8000 * 4096 * 2
     assert b["ep_regroup_back"] == 2 * 8000 * 4096 * 4
+
+
+def test_measured_traffic_entry():
+    # the gate/up GEMM's DRAM bytes from a one-launch ncu capture (read +
+    # write), stored with the fingerprint of the kernel sources it was taken
+    # on: within 5 % of the launch's algorithmic bytes (no weight tile
+    # fetched twice), and the fingerprint well formed and reproducible
+    for key, algorithmic in ((("mixtral_prefill", "gate_up"), 2181038080),
+                             (("mixtral_prefill", "down"), None)):
+        traffic, fp = bench.MEASURED_TRAFFIC[key]
+        assert traffic > 0
+        if algorithmic is not None:
+            assert traffic <= 1.05 * algorithmic
+        assert len(fp) == 16 and int(fp, 16) >= 0
+    assert bench.kernel_fingerprint() == bench.kernel_fingerprint()
