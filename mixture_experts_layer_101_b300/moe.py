@@ -314,9 +314,10 @@ def moe_route(cfg: LayerConfig, x, w_r, b_r, idx, gate, stats: Stats | None, ws,
 def moe_route_no_workspace(cfg: LayerConfig, x, w_r, b_r, idx, gate, stats: Stats | None,
                            stream=None):
     """moe_route without a workspace: for callers that cannot allocate device
-    memory. It always runs the CUDA-core router (moe_route takes the tensor-
-    core router for bf16 layers with d % 64 == 0, so the two can choose
-    differently on near-tie tokens). The library keeps the statistics'
+    memory. It always runs a CUDA-core router (moe_route takes the tensor-
+    core router for bf16 layers with d % 64 == 0 beyond 128 tokens or 32
+    experts, so the two can choose differently on near-tie tokens; below
+    that both run the small-batch router). The library keeps the statistics'
     partial sums in a fixed 1 MiB array (ceil(T/32) * (N + 2) <= 131072,
     else MOE_ERR_WORKSPACE); calls share it, so calls that overlap on the GPU
     must not be issued. The first call in a CUDA context (normally once per
